@@ -1,0 +1,138 @@
+"""Planted mistakes: each copy of the oracle below carries one plausible
+error, and at least one of the pins used on the real oracle must reject it.
+This shows the pins are strong enough to catch a dropped term, a wrong sign,
+a transposed operand, a wrong view, a wrong normalisation or a wrong
+tie-break -- on the CPU, never on a GPU.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import ns as ons
+from oracle import planning as op
+from test_oracle_ns import A, B, C, EPS, svd_closed_form, scalar_map, rel
+from test_oracle_planning import load
+
+
+def ns_variant(t, k, a, b, c, eps, *, view="first", gram="xxt", norm="fro_plus",
+               back=True, steps_off=0, order="poly_x"):
+    t = np.asarray(t, dtype=np.float64)
+    shape = t.shape
+    if view == "first":
+        g = t.reshape(shape[0], -1)
+    else:                                   # mistake: last dim as cols
+        g = t.reshape(-1, shape[-1])
+    tr = g.shape[0] > g.shape[1]
+    x = g.T if tr else g
+    nrm = math.sqrt(float(np.sum(x * x)))
+    if norm == "fro_plus":
+        x = x / (nrm + eps)
+    elif norm == "fro_max":
+        x = x / max(nrm, eps)
+    elif norm == "spectral":
+        x = x / (np.linalg.norm(x, 2) + eps)
+    for _ in range(k + steps_off):
+        gm = x @ x.T if gram == "xxt" else x.T @ x
+        p = b * gm + c * (gm @ gm)
+        if order == "poly_x":
+            x = a * x + p @ x
+        else:                                # mistake: a folded into the wrong place
+            x = (a * gm + p) @ x
+    if tr and back:
+        x = x.T
+    return x.reshape(shape) if x.size == t.size and (not tr or back) else x
+
+
+def pins_pass(fn) -> bool:
+    """Run the NS pins against `fn`; True iff every pin passes."""
+    rng = np.random.default_rng(123)
+    try:
+        for shape in [(40, 70), (70, 40), (32, 32), (8, 3, 2, 2)]:
+            t = rng.standard_normal(shape)
+            got = np.asarray(fn(t, 5, A, B, C, EPS))
+            if got.shape != t.shape or rel(got, svd_closed_form(t, 5)) > 1e-10:
+                return False
+        t = rng.standard_normal((12, 20))
+        t *= 1e-7 / np.linalg.norm(t)
+        if rel(fn(t, 5, A, B, C, EPS), svd_closed_form(t, 5)) > 1e-10:
+            return False
+        d = [1.0, 0.5, 0.1]
+        t = np.zeros((3, 5))
+        for i, v in enumerate(d):
+            t[i, i] = v
+        nu = math.sqrt(sum(v * v for v in d)) + EPS
+        got = fn(t, 5, A, B, C, EPS)
+        for i, v in enumerate(d):
+            if abs(got[i, i] - scalar_map(v / nu, 5)) > 1e-13:
+                return False
+    except Exception:
+        return False
+    return True
+
+
+def test_real_oracle_passes_pins():
+    assert pins_pass(ons.newton_schulz)
+
+
+MUTANTS = {
+    "dropped c*A@A term": lambda t, k, a, b, c, e: ons.newton_schulz(t, k, a, b, 0.0, e),
+    "wrong sign of b": lambda t, k, a, b, c, e: ons.newton_schulz(t, k, a, -b, c, e),
+    "a and b swapped": lambda t, k, a, b, c, e: ons.newton_schulz(t, k, b, a, c, e),
+    "one step short": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, steps_off=-1),
+    "Gram as X^T X": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, gram="xtx"),
+    "no transpose back": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, back=False),
+    "view as (prod(shape[:-1]), shape[-1])": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, view="last"),
+    "max(norm, eps) normalisation": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, norm="fro_max"),
+    "spectral-norm normalisation": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, norm="spectral"),
+    "a multiplies A instead of X": lambda t, k, a, b, c, e: ns_variant(t, k, a, b, c, e, order="a_gram"),
+}
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_ns_mutant_is_caught(name):
+    assert not pins_pass(MUTANTS[name])
+
+
+def lpt_variant(works, *, ascending=False, singles_first=True, last_on_tie=False, reverse_ties=False):
+    load_ = {}
+    for w in works:
+        for r in w.candidates:
+            load_.setdefault(r, 0)
+    single = [w for w in works if len(w.candidates) == 1] if singles_first else []
+    multi = [w for w in works if not singles_first or len(w.candidates) > 1]
+    if reverse_ties:
+        multi = list(reversed(multi))
+    multi.sort(key=lambda w: w.cost if ascending else -w.cost)
+    out = {}
+    for w in single + multi:
+        best = w.candidates[0]
+        for r in w.candidates[1:]:
+            if load_[r] < load_[best] or (last_on_tie and load_[r] == load_[best]):
+                best = r
+        out[w.tensor_index] = best
+        load_[best] += w.cost
+    return out
+
+
+def lpt_pins_pass(fn) -> bool:
+    for case in load("planning_hand_cases.json")["lpt"]:
+        works = [op.OwnerWork(i, c, cand) for i, (c, cand) in enumerate(zip(case["costs"], case["candidates"]))]
+        got = fn(works)
+        if [got[i] for i in range(len(case["costs"]))] != case["owners"]:
+            return False
+    return True
+
+
+def test_real_lpt_passes_pins():
+    assert lpt_pins_pass(op.assign_owner_work)
+    assert lpt_pins_pass(lpt_variant)
+
+
+@pytest.mark.parametrize("kw", [dict(ascending=True), dict(singles_first=False),
+                                dict(last_on_tie=True), dict(reverse_ties=True)],
+                         ids=["ascending cost", "no single-candidate pass", "last rank on load tie",
+                              "reverse index on cost tie"])
+def test_lpt_mutant_is_caught(kw):
+    assert not lpt_pins_pass(lambda w: lpt_variant(w, **kw))
