@@ -1,0 +1,200 @@
+/*
+ * nsgb300 -- shape-batched quintic Newton-Schulz for GB300 (sm_103a), with the
+ * shard -> home pack and home -> shard unpack around it.
+ *
+ * C ABI of libnsgb300.so. Every function returns an int status (NS_OK = 0 or
+ * a negative NS_ERR_* code), never throws and never aborts the process.
+ * Device buffers are plain device pointers owned by the caller; the library
+ * owns only the plan (host metadata plus, for pack/unpack, a small device
+ * routing table it allocates on the first pack/unpack call on a device).
+ * Asynchronous work is ordered on the `stream` argument (a cudaStream_t passed
+ * as void*; NULL = the legacy default stream). Errors found on the device
+ * (a bounded wait that ran out, an index a kernel refused) are recorded in a
+ * device status word and reported by ns_check_status().
+ *
+ * Sources (page title, entry):
+ *  [LSA]  Megatron-Core API, core.optimizer.layer_sharded_a2a:
+ *         params_by_home, route_to_ns_home, route_from_ns_home.
+ *  [OP]   Megatron-Core API, core.distributed.fsdp.src.megatron_fsdp.
+ *         experimental.owner_planning: select_ge_2d_params, ns_cost_fn,
+ *         _OwnerWork, assign_owner_work, GroupOwnerLayout, OwnerGatherPlan,
+ *         OwnerScatterPlan.
+ *  [ISS]  Megatron-LM issue #6720 "[GTP][Muon] Optimize Muon step
+ *         performance": shape-batched NS, SYRK symmetric kernels,
+ *         fp32/TF32 Gram + trace ridge.
+ */
+#ifndef NSGB300_H
+#define NSGB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+enum {
+  NS_OK = 0,
+  NS_ERR_ARG = -1,           /* null pointer, bad count, S/shard_dim mismatch   */
+  NS_ERR_SHAPE = -2,         /* ndim < 2 for a participating tensor, bad dims   */
+  NS_ERR_NOT_DIVISIBLE = -3, /* shard_dim size (or buffer size) not divisible by S */
+  NS_ERR_HOME = -4,          /* home/owner missing, out of range, or not a holder */
+  NS_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed               */
+  NS_ERR_TIMEOUT = -6,       /* a kernel's bounded wait ran out (device status)  */
+  NS_ERR_DEVICE_CHECK = -7,  /* a kernel refused an out-of-range index           */
+  NS_ERR_UNSUPPORTED = -8,   /* mode or device not supported by this build      */
+  NS_ERR_WORKSPACE = -9      /* workspace missing, too small or misaligned       */
+};
+
+/* Precision policy of a plan (gram_mode). */
+enum {
+  NS_BF16 = 0,      /* bf16 X, A, B operands, fp32 accumulation and epilogues; bf16 in, bf16 out */
+  NS_FP32_GRAM = 1  /* fp32 X, A, B: TF32 Gram, split-TF32 A*A and B*X; bf16 in, fp32 out */
+};
+
+/* Data model of a plan. */
+enum {
+  NS_LAYOUT_ROW_SHARD = 0, /* [LSA] every rank holds a (P/S, Q) slice of every param    */
+  NS_LAYOUT_FLAT = 1       /* [OP]  one flat buffer split evenly into S rank ranges     */
+};
+
+typedef struct ns_plan ns_plan_t; /* opaque; owned by the library */
+
+/* ------------------------------------------------------------- host only */
+
+/* [OP] ns_cost_fn. View `shape` (ndim >= 2) as (rows, cols) = (shape[0],
+ * prod(shape[1:])); cost = rows*cols*(min(rows, cols)*steps + 1), exact in
+ * int64. NS_ERR_SHAPE if ndim < 2 or a dim is negative; NS_ERR_ARG on null
+ * pointers, steps < 0, or int64 overflow. */
+int ns_cost(const int64_t* shape, int ndim, int steps, int64_t* cost_out);
+
+/* [OP] assign_owner_work: greedy LPT. Tensors with one candidate are taken
+ * first in index order, then the rest in descending cost (equal costs keep
+ * index order); each goes to its least-loaded candidate, equal loads to the
+ * candidate listed first. Candidates of tensor i are
+ * cand_idx[cand_ptr[i] .. cand_ptr[i+1]) (CSR), ranks in [0, n_ranks), listed
+ * in buffer order. owner_out[i] receives the owner. NS_ERR_HOME if a tensor
+ * has no candidate or a candidate is out of range; NS_ERR_ARG on bad
+ * arguments (costs must be > 0). */
+int ns_assign_owner_work(int n_tensors, const int64_t* costs, const int32_t* cand_ptr,
+                         const int32_t* cand_idx, int n_ranks, int32_t* owner_out);
+
+/* [LSA] route_to_ns_home / route_from_ns_home plan cache, [OP] ns_cost_fn.
+ * Row-shard plan over n_tensors params; tensor i has ndims[i] dims, listed
+ * consecutively in shapes_flat. Every param is sharded S ways along
+ * shard_dim (its size there must be divisible by S: NS_ERR_NOT_DIVISIBLE).
+ * home_of[i] in [0, S) is param i's NS home; NULL asks for LPT homes over all
+ * S ranks with cost ns_cost(shape, steps). steps >= 0; (a, b, c) are the
+ * quintic coefficients used in every step; eps is added to the Frobenius
+ * norm; ridge >= 0 adds ridge*(trace(A)/m)*I to A before B is formed (only
+ * in NS_FP32_GRAM mode; must be 0 in NS_BF16 mode). The plan copies every
+ * input array; the caller owns its validity only in the sense of [LSA]:
+ * reuse it only while shapes, homes and S are unchanged. No CUDA call. */
+int ns_plan_create(int n_tensors, const int32_t* ndims, const int64_t* shapes_flat, int steps,
+                   float a, float b, float c, float eps, int gram_mode, float ridge, int S,
+                   int shard_dim, const int32_t* home_of, ns_plan_t** plan_out);
+
+/* [OP] GroupOwnerLayout / OwnerGatherPlan data model. Flat-buffer plan: tensor
+ * i occupies elements [offsets[i], offsets[i] + numel_i) of a buffer of
+ * buffer_size elements (buffer_size % S == 0, else NS_ERR_NOT_DIVISIBLE);
+ * rank r holds [r*size/S, (r+1)*size/S). participating[i] != 0 marks the
+ * tensors that take part (NULL = every tensor with ndim >= 2, the
+ * select_ge_2d_params default); participating tensors must not overlap and
+ * must have ndim >= 2 and numel > 0. owner_of[i] (read for participating i
+ * only) must be a rank holding part of tensor i (NS_ERR_HOME otherwise);
+ * NULL asks for assign_owner_work's default LPT owners. Other arguments as
+ * in ns_plan_create. No CUDA call. */
+int ns_plan_create_flat(int n_tensors, const int32_t* ndims, const int64_t* shapes_flat,
+                        const int64_t* offsets, int64_t buffer_size, const uint8_t* participating,
+                        int steps, float a, float b, float c, float eps, int gram_mode, float ridge,
+                        int S, const int32_t* owner_of, ns_plan_t** plan_out);
+
+/* Frees the plan and any device routing tables it uploaded. NULL is a no-op. */
+int ns_plan_destroy(ns_plan_t* plan);
+
+/* Plan summary: info[0] = n_tensors, [1] = participating count, [2] = S,
+ * [3] = layout, [4] = gram_mode, [5] = steps, [6] = number of shape
+ * buckets, [7] = per-rank buffer elements (row-shard) or buffer_size/S (flat),
+ * [8] = input element bytes, [9] = output element bytes. info has >= 10 slots. */
+int ns_plan_info(const ns_plan_t* plan, int64_t* info);
+
+/* [LSA] params_by_home source: home_out[i] = home (owner) of tensor i, or -1
+ * for a tensor that does not participate. home_out has n_tensors slots. */
+int ns_plan_homes(const ns_plan_t* plan, int32_t* home_out);
+
+/* Layout of the home buffers: home_offsets[i] = element offset of tensor i in
+ * its home buffer (-1 if not participating); home_sizes[h] = elements in home
+ * buffer h; rank_sizes[r] = elements in rank buffer r. Any pointer may be
+ * NULL. Home h holds its tensors complete, in increasing index order. */
+int ns_plan_home_layout(const ns_plan_t* plan, int64_t* home_offsets, int64_t* home_sizes,
+                        int64_t* rank_sizes);
+
+/* Bytes of device workspace ns_orthogonalize_batched needs (256-byte
+ * aligned base required). Zero when nothing participates. */
+int ns_plan_workspace_bytes(const ns_plan_t* plan, uint64_t* bytes);
+
+/* [OP] OwnerGatherPlan metadata seen from rank rho (flat plans only, else
+ * NS_ERR_ARG). send_sizes[o] = elements rho sends to owner o (0 = absent,
+ * always 0 for o == rho); recv_sizes[s] = elements rho receives from s;
+ * recv_offsets[i*S + s] = offset of tensor i's piece inside s's buffer to rho
+ * (-1 = absent); own_sizes[i] = elements of rho's own shard of tensor i if
+ * rho owns i, else -1. Any output pointer may be NULL. */
+int ns_owner_gather_meta(const ns_plan_t* plan, int rho, int64_t* send_sizes, int64_t* recv_sizes,
+                         int64_t* recv_offsets, int64_t* own_sizes);
+
+/* [OP] OwnerScatterPlan metadata seen from rank rho (flat plans only):
+ * send_sizes[d] = result elements rho (as owner) sends to d; recv_sizes[o]
+ * = elements rho receives from owner o; recv_offsets[i*S + o] = offset of
+ * tensor i's result piece inside o's buffer to rho (-1 = absent). */
+int ns_owner_scatter_meta(const ns_plan_t* plan, int rho, int64_t* send_sizes, int64_t* recv_sizes,
+                          int64_t* recv_offsets);
+
+const char* ns_status_string(int status);
+
+/* ----------------------------------------------------------------- device */
+
+/* [OP] ns_cost_fn step, [ISS] shape-batched NS. Orthogonalises the n
+ * participating tensors of the plan (n must equal the participating count),
+ * in index order: in[j] / out[j] are device pointers to the j-th participating
+ * tensor, contiguous row-major in its original shape (bf16 in; bf16 out in
+ * NS_BF16 mode, fp32 out in NS_FP32_GRAM mode). out[j] == in[j] is allowed;
+ * other overlaps are not. Each tensor is viewed as (shape[0], prod(shape[1:])),
+ * transposed so rows <= cols, scaled by 1/(||X||_F + eps), run for `steps`
+ * steps of A = X X^T; X = a X + (b A + c A A) X, transposed back and stored.
+ * workspace must hold ns_plan_workspace_bytes() bytes, 256-byte aligned; it
+ * is scratch (no contents kept between calls). Asynchronous on `stream`;
+ * calls that share a workspace must not overlap on the GPU. */
+int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const* out, int n,
+                             void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* [LSA] route_to_ns_home, [OP] OwnerGatherPlan.pack + reconstruct_full.
+ * Device-local gather over S simulated ranks (no collective): rank_bufs[r]
+ * (S device pointers, input dtype) hold rank r's data -- row-shard plans: its
+ * (P/S, Q) shard of every param, in index order; flat plans: elements
+ * [r*size/S, (r+1)*size/S) of the flat buffer. home_bufs[h] (S pointers)
+ * receive home h's complete tensors in increasing index order, at the offsets
+ * ns_plan_home_layout reports. S and shard_dim must equal the plan's (flat
+ * plans: shard_dim 0). Bit-exact copy. The first pack/unpack call on a device
+ * uploads the plan's routing table (cudaMalloc + copy): make it before any
+ * stream capture. */
+int ns_pack_to_home(ns_plan_t* plan, const void* const* rank_bufs, int S, int shard_dim,
+                    void* const* home_bufs, void* stream);
+
+/* [LSA] route_from_ns_home, [OP] OwnerScatterPlan.pack + unpack. Inverse of
+ * ns_pack_to_home on the output dtype: home_bufs[h] hold complete results,
+ * rank_bufs[r] receive rank r's shard of every result (flat plans: only the
+ * elements of participating tensors are written). */
+int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, int shard_dim,
+                        void* const* rank_bufs, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: NS_ERR_TIMEOUT or NS_ERR_DEVICE_CHECK if a kernel recorded one, else
+ * NS_ERR_CUDA on a pending CUDA error, else NS_OK. plan may be NULL. */
+int ns_check_status(ns_plan_t* plan, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSGB300_H */

@@ -1,0 +1,104 @@
+// Launch parameters shared by the host orchestration (api.cu) and the kernels
+// (gemm.cu, prologue.cu, pack.cu), and the launcher entry points. Everything a
+// kernel needs per call travels by value in its parameter block, so the
+// Newton-Schulz path itself allocates nothing.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nsk {
+
+// ------------------------------------------------------------------- GEMMs
+constexpr int GEMM_MAX_BUCKETS = 8;
+enum GemmPhase { PH_GRAM = 0, PH_A2B = 1, PH_BX = 2 };
+
+struct GemmBucket {
+  long long tile_begin;  // first global tile index of this bucket
+  long long out_stride;  // elements between consecutive matrices of `out`
+  long long aux_stride;  // elements between consecutive matrices of `aux`
+  void* out;             // bf16: A (Gram), B (A2B), X_next (BX)
+  const void* aux;       // bf16: A (A2B), X_cur (BX), unused (Gram)
+  int count;             // matrices in the bucket
+  int tiles_m, tiles_n;  // tile grid of one output matrix
+  int tiles_per_mat;     // tiles computed per matrix (upper ones only for SYRK)
+  int k_blocks;          // K / 64
+  int ld_out, ld_aux;    // leading dimensions (elements)
+  int cols_valid;        // output columns that exist (m_pad or n_pad)
+};
+
+struct alignas(64) GemmParams {
+  CUtensorMap tma[GEMM_MAX_BUCKETS];  // A operand, K-major, box {64, 128, 1}
+  CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} / MN-major box {64,64,1}
+  GemmBucket bk[GEMM_MAX_BUCKETS];
+  long long total_tiles;
+  int nb;
+  float alpha, beta, gamma;  // a, b, c of the quintic step
+  unsigned int* status;
+};
+
+constexpr int GEMM_BM = 128, GEMM_BN = 256, GEMM_BK = 64;
+
+// ------------------------------------------------------- prologue / store
+constexpr int PRO_MAX_MATS = 192;
+
+struct MatDesc {
+  const void* in;       // original tensor, row-major (rows x cols), bf16
+  void* out;            // result, row-major (rows x cols)
+  void* x;              // this matrix's X_0 in the workspace (m_pad x n_pad, bf16)
+  const void* xfinal;   // this matrix's X_k in the workspace
+  float* partial;       // nchunks partial sums of squares
+  float* scale;         // 1 / (||X||_F + eps)
+  long long numel;
+  int rows, cols;
+  int transposed;
+};
+
+struct ProParams {
+  MatDesc md[PRO_MAX_MATS];
+  int count;
+  int nchunks;          // sum-of-squares chunks per matrix (same for the batch)
+  int m_pad, n_pad;     // workspace matrix dims (same for the batch)
+  int m, n;             // valid dims after the transpose
+  float eps;
+  int out_f32;          // result dtype: 0 bf16, 1 fp32
+  unsigned int* status;
+};
+
+// ----------------------------------------------------------- pack / unpack
+constexpr int ROUTE_MAX_RANKS = 64;
+
+struct RouteEntry {
+  long long seg_begin;  // first position of the tensor in the rank coordinate space
+  long long seg_len;    // positions it occupies there
+  long long home_off;   // element offset of the complete tensor in its home buffer
+  long long inner;      // row-shard: contiguous run inside a shard (D/S * post)
+  long long outer;      // row-shard: stride between runs in the full tensor (D * post)
+  int home;
+  int pad;
+};
+
+struct PackParams {
+  void* rank_ptr[ROUTE_MAX_RANKS];
+  void* home_ptr[ROUTE_MAX_RANKS];
+  const RouteEntry* entries;
+  long long n_entries;
+  long long rank_len;   // positions per rank buffer
+  long long chunk;      // positions per CTA
+  int S;
+  int flat;             // 1: flat-buffer model, 0: row-shard model
+  int elem_bytes;       // 2 or 4
+  int to_home;          // 1: pack (rank -> home), 0: unpack (home -> rank)
+  unsigned int* status;
+};
+
+// ----------------------------------------------------------------- launchers
+cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st);
+cudaError_t launch_scale(const ProParams& p, cudaStream_t st);
+cudaError_t launch_prep(const ProParams& p, cudaStream_t st);
+cudaError_t launch_store(const ProParams& p, cudaStream_t st);
+cudaError_t launch_pack(const PackParams& p, cudaStream_t st);
+
+}  // namespace nsk
