@@ -1,0 +1,399 @@
+// Device-side C ABI: shape-batched Newton-Schulz orchestration, pack/unpack,
+// the device status word, and plan destruction.
+//
+// ns_orthogonalize_batched follows the Megatron-Core API page owner_planning
+// (ns_cost_fn: view, normalise, transpose so rows <= cols, then per step
+// A = X X^T; X = a X + (b A + c A A) X) and the Megatron-LM issue #6720
+// ("shape-batched NS", "SYRK symmetric kernels"): tensors of equal (m, n)
+// form a bucket laid out as one [count, m_pad, n_pad] array in the caller's
+// workspace, and every phase of every step runs as one persistent launch over
+// the tiles of all buckets. Nothing here allocates device memory; all
+// per-call data travels in kernel parameter blocks.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/nsgb300.h"
+#include "kernels.h"
+#include "plan.h"
+#include "status.h"
+
+// Device status word (one per device context): kernels atomicOr NS_DEV_* bits.
+__device__ unsigned int g_ns_status;
+
+namespace {
+
+using nsplan::Bucket;
+using nsplan::Plan;
+using nsplan::Tensor;
+
+std::mutex g_mu;
+unsigned int* g_status_ptr[nsplan::kMaxDevices] = {nullptr};
+int g_sm_count[nsplan::kMaxDevices] = {0};
+int g_cc_ok[nsplan::kMaxDevices] = {0};  // 0 unknown, 1 sm_103, -1 other
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: status word address, SM count, architecture check.
+int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NS_ERR_CUDA;
+  if (dev < 0 || dev >= nsplan::kMaxDevices) return NS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_cc_ok[dev] == 0) {
+    int major = 0, minor = 0, nsm = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NS_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      g_cc_ok[dev] = -1;
+      return NS_ERR_UNSUPPORTED;
+    }
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_ns_status) != cudaSuccess) return NS_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned int*>(sp);
+    g_sm_count[dev] = nsm;
+    g_cc_ok[dev] = 1;
+  }
+  if (g_cc_ok[dev] < 0) return NS_ERR_UNSUPPORTED;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return NS_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *dev_out = dev;
+  *status_out = g_status_ptr[dev];
+  *nsm_out = g_sm_count[dev];
+  return NS_OK;
+}
+
+// 3-D bf16 tensor map over [count][outer][inner] with a {box_inner, box_outer, 1}
+// box, 128-byte swizzle, zero fill outside the array.
+int make_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count, uint32_t box_inner,
+             uint32_t box_outer) {
+  cuuint64_t dims[3] = {inner, outer, count};
+  cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
+}
+
+long long syrk_tiles(int tiles_m, int tiles_n) {
+  long long t = 0;
+  for (int tm = 0; tm < tiles_m; ++tm) t += tiles_n - (tm * nsk::GEMM_BM) / nsk::GEMM_BN;
+  return t;
+}
+
+struct BucketPtrs {
+  char* x0;
+  char* x1;
+  char* a;
+  char* b;
+  float* partial;
+  float* scale;
+};
+
+BucketPtrs bucket_ptrs(const Bucket& b, char* ws) {
+  BucketPtrs q;
+  q.x0 = ws + b.off_x0;
+  q.x1 = ws + b.off_x1;
+  q.a = ws + b.off_a;
+  q.b = ws + b.off_b;
+  q.partial = reinterpret_cast<float*>(ws + b.off_partial);
+  q.scale = reinterpret_cast<float*>(ws + b.off_scale);
+  return q;
+}
+
+// One launch of `phase` over buckets [b0, b1). `cur_is_x0` selects the X buffer
+// the step reads.
+int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
+              unsigned int* status, cudaStream_t st) {
+  nsk::GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  gp.alpha = p.a;
+  gp.beta = p.b;
+  gp.gamma = p.c;
+  gp.status = status;
+  long long tiles = 0;
+  int nb = 0;
+  for (size_t bi = b0; bi < b1; ++bi, ++nb) {
+    const Bucket& b = p.buckets[bi];
+    const BucketPtrs q = bucket_ptrs(b, ws);
+    char* cur = cur_is_x0 ? q.x0 : q.x1;
+    char* nxt = cur_is_x0 ? q.x1 : q.x0;
+    const uint64_t cnt = b.members.size();
+    nsk::GemmBucket& g = gp.bk[nb];
+    g.tile_begin = tiles;
+    g.count = static_cast<int>(cnt);
+    g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
+    int rc = NS_OK;
+    if (phase == nsk::PH_GRAM || phase == nsk::PH_A2B) {
+      g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
+      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
+      g.cols_valid = static_cast<int>(b.m_pad);
+      g.ld_out = static_cast<int>(b.m_pad);
+      g.out_stride = b.m_pad * b.m_pad;
+      if (phase == nsk::PH_GRAM) {
+        g.k_blocks = static_cast<int>(b.n_pad / nsk::GEMM_BK);
+        g.out = q.a;
+        g.aux = nullptr;
+        rc = make_map(&gp.tma[nb], cur, b.n_pad, b.m_pad, cnt, 64, 128);
+        if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 128);
+      } else {
+        g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM_BK);
+        g.out = q.b;
+        g.aux = q.a;
+        g.ld_aux = static_cast<int>(b.m_pad);
+        g.aux_stride = b.m_pad * b.m_pad;
+        rc = make_map(&gp.tma[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
+        if (rc == NS_OK) rc = make_map(&gp.tmb[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
+      }
+    } else {
+      g.tiles_n = static_cast<int>((b.n_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
+      g.tiles_per_mat = g.tiles_m * g.tiles_n;
+      g.cols_valid = static_cast<int>(b.n_pad);
+      g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM_BK);
+      g.out = nxt;
+      g.aux = cur;
+      g.ld_out = static_cast<int>(b.n_pad);
+      g.ld_aux = static_cast<int>(b.n_pad);
+      g.out_stride = b.m_pad * b.n_pad;
+      g.aux_stride = b.m_pad * b.n_pad;
+      rc = make_map(&gp.tma[nb], q.b, b.m_pad, b.m_pad, cnt, 64, 128);
+      if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 64);
+    }
+    if (rc != NS_OK) return rc;
+    tiles += static_cast<long long>(g.tiles_per_mat) * static_cast<long long>(cnt);
+  }
+  gp.nb = nb;
+  gp.total_tiles = tiles;
+  const int grid = static_cast<int>(std::min<long long>(tiles, nsm));
+  return nsk::launch_gemm(phase, gp, grid, st) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
+
+int upload_route(Plan& p, int dev) {
+  if (p.d_route[dev] || p.route.empty()) return NS_OK;
+  const size_t bytes = p.route.size() * sizeof(nsk::RouteEntry);
+  void* d = nullptr;
+  if (cudaMalloc(&d, bytes) != cudaSuccess) return NS_ERR_CUDA;
+  if (cudaMemcpy(d, p.route.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(d);
+    return NS_ERR_CUDA;
+  }
+  p.d_route[dev] = d;
+  return NS_OK;
+}
+
+int route(ns_plan_t* plan, void* const* rank_bufs, void* const* home_bufs, int S, int shard_dim, bool to_home,
+          int elem_bytes, cudaStream_t st) {
+  if (!plan) return NS_ERR_ARG;
+  Plan& p = plan->p;
+  if (S != p.S) return NS_ERR_ARG;
+  if (p.layout == NS_LAYOUT_ROW_SHARD ? shard_dim != p.shard_dim : shard_dim != 0) return NS_ERR_ARG;
+  if (p.route.empty() || p.rank_len == 0) return NS_OK;
+  if (!rank_bufs || !home_bufs) return NS_ERR_ARG;
+  for (int r = 0; r < S; ++r) {
+    if (!rank_bufs[r] && p.rank_len > 0) return NS_ERR_ARG;
+    if (!home_bufs[r] && p.home_sizes[r] > 0) return NS_ERR_ARG;
+  }
+  int dev;
+  unsigned int* status;
+  int nsm;
+  int rc = device_setup(&dev, &status, &nsm);
+  if (rc != NS_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    rc = upload_route(p, dev);
+  }
+  if (rc != NS_OK) return rc;
+  nsk::PackParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  for (int r = 0; r < S; ++r) {
+    pp.rank_ptr[r] = rank_bufs[r];
+    pp.home_ptr[r] = home_bufs[r];
+  }
+  pp.entries = static_cast<const nsk::RouteEntry*>(p.d_route[dev]);
+  pp.n_entries = static_cast<long long>(p.route.size());
+  pp.rank_len = p.rank_len;
+  pp.chunk = 32768;
+  pp.S = S;
+  pp.flat = p.layout == NS_LAYOUT_FLAT ? 1 : 0;
+  pp.elem_bytes = elem_bytes;
+  pp.to_home = to_home ? 1 : 0;
+  pp.status = status;
+  return nsk::launch_pack(pp, st) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const* out, int n, void* workspace,
+                             uint64_t workspace_bytes, void* stream) {
+  if (!plan) return NS_ERR_ARG;
+  Plan& p = plan->p;
+  if (n != static_cast<int>(p.part.size())) return NS_ERR_ARG;
+  if (n == 0) return NS_OK;
+  if (!in || !out) return NS_ERR_ARG;
+  for (int j = 0; j < n; ++j) {
+    const Tensor& t = p.t[p.part[j]];
+    if (t.numel > 0 && (!in[j] || !out[j])) return NS_ERR_ARG;
+  }
+  if (p.gram_mode != NS_BF16) return NS_ERR_UNSUPPORTED;
+  if (p.buckets.empty()) return NS_OK;
+  if (!workspace || workspace_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return NS_ERR_WORKSPACE;
+  int dev;
+  unsigned int* status;
+  int nsm;
+  int rc = device_setup(&dev, &status, &nsm);
+  if (rc != NS_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+
+  // prologue: sums of squares, scales, X_0 = scale * (T or T^T), zero padded
+  for (const Bucket& b : p.buckets) {
+    const BucketPtrs q = bucket_ptrs(b, ws);
+    const size_t cnt = b.members.size();
+    for (size_t s0 = 0; s0 < cnt; s0 += nsk::PRO_MAX_MATS) {
+      nsk::ProParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.count = static_cast<int>(std::min<size_t>(nsk::PRO_MAX_MATS, cnt - s0));
+      pp.nchunks = static_cast<int>(b.nchunks);
+      pp.m_pad = static_cast<int>(b.m_pad);
+      pp.n_pad = static_cast<int>(b.n_pad);
+      pp.m = static_cast<int>(b.m);
+      pp.n = static_cast<int>(b.n);
+      pp.eps = p.eps;
+      pp.out_f32 = 0;
+      pp.status = status;
+      for (int k = 0; k < pp.count; ++k) {
+        const size_t s = s0 + k;
+        const Tensor& t = p.t[b.members[s]];
+        nsk::MatDesc& d = pp.md[k];
+        d.in = in[t.ordinal];
+        d.out = out[t.ordinal];
+        d.x = q.x0 + s * b.m_pad * b.n_pad * 2;
+        d.partial = q.partial + s * b.nchunks;
+        d.scale = q.scale + s;
+        d.numel = t.numel;
+        d.rows = static_cast<int>(t.rows);
+        d.cols = static_cast<int>(t.cols);
+        d.transposed = t.transposed ? 1 : 0;
+      }
+      if (nsk::launch_sumsq(pp, st) != cudaSuccess || nsk::launch_scale(pp, st) != cudaSuccess ||
+          nsk::launch_prep(pp, st) != cudaSuccess)
+        return NS_ERR_CUDA;
+    }
+  }
+  // k steps x (Gram, A*A + B, B*X) over all buckets
+  bool cur_is_x0 = true;
+  for (int step = 0; step < p.steps; ++step) {
+    for (int phase = nsk::PH_GRAM; phase <= nsk::PH_BX; ++phase) {
+      for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
+        const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
+        rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, st);
+        if (rc != NS_OK) return rc;
+      }
+    }
+    cur_is_x0 = !cur_is_x0;
+  }
+  // transpose back and store
+  for (const Bucket& b : p.buckets) {
+    const BucketPtrs q = bucket_ptrs(b, ws);
+    const char* xf = cur_is_x0 ? q.x0 : q.x1;
+    const size_t cnt = b.members.size();
+    for (size_t s0 = 0; s0 < cnt; s0 += nsk::PRO_MAX_MATS) {
+      nsk::ProParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.count = static_cast<int>(std::min<size_t>(nsk::PRO_MAX_MATS, cnt - s0));
+      pp.m_pad = static_cast<int>(b.m_pad);
+      pp.n_pad = static_cast<int>(b.n_pad);
+      pp.m = static_cast<int>(b.m);
+      pp.n = static_cast<int>(b.n);
+      pp.out_f32 = p.out_bytes == 4 ? 1 : 0;
+      pp.status = status;
+      for (int k = 0; k < pp.count; ++k) {
+        const size_t s = s0 + k;
+        const Tensor& t = p.t[b.members[s]];
+        nsk::MatDesc& d = pp.md[k];
+        d.out = out[t.ordinal];
+        d.xfinal = xf + s * b.m_pad * b.n_pad * 2;
+        d.rows = static_cast<int>(t.rows);
+        d.cols = static_cast<int>(t.cols);
+        d.transposed = t.transposed ? 1 : 0;
+        d.numel = t.numel;
+      }
+      if (nsk::launch_store(pp, st) != cudaSuccess) return NS_ERR_CUDA;
+    }
+  }
+  return NS_OK;
+}
+
+int ns_pack_to_home(ns_plan_t* plan, const void* const* rank_bufs, int S, int shard_dim, void* const* home_bufs,
+                    void* stream) {
+  return route(plan, const_cast<void* const*>(rank_bufs), home_bufs, S, shard_dim, true,
+               plan ? plan->p.in_bytes : 2, static_cast<cudaStream_t>(stream));
+}
+
+int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, int shard_dim, void* const* rank_bufs,
+                        void* stream) {
+  return route(plan, rank_bufs, const_cast<void* const*>(home_bufs), S, shard_dim, false,
+               plan ? plan->p.out_bytes : 2, static_cast<cudaStream_t>(stream));
+}
+
+int ns_check_status(ns_plan_t* /*plan*/, void* stream) {
+  int dev;
+  unsigned int* status;
+  int nsm;
+  int rc = device_setup(&dev, &status, &nsm);
+  if (rc != NS_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NS_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return NS_ERR_CUDA;
+  if (word) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return NS_ERR_CUDA;
+    if (word & NS_DEV_TIMEOUT) return NS_ERR_TIMEOUT;
+    return NS_ERR_DEVICE_CHECK;
+  }
+  if (cudaGetLastError() != cudaSuccess) return NS_ERR_CUDA;
+  return NS_OK;
+}
+
+int ns_plan_destroy(ns_plan_t* plan) {
+  if (!plan) return NS_OK;
+  bool any = false;
+  for (int d = 0; d < nsplan::kMaxDevices; ++d) any = any || plan->p.d_route[d] != nullptr;
+  if (!any) {
+    delete plan;
+    return NS_OK;
+  }
+  int cur = -1;
+  const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;
+  for (int d = 0; d < nsplan::kMaxDevices; ++d) {
+    if (!plan->p.d_route[d]) continue;
+    if (cudaSetDevice(d) == cudaSuccess) cudaFree(plan->p.d_route[d]);
+    plan->p.d_route[d] = nullptr;
+  }
+  if (have_dev) cudaSetDevice(cur);
+  delete plan;
+  return NS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,318 @@
+// The three tensor-core products of one quintic Newton-Schulz step
+// (Megatron-Core API page owner_planning, ns_cost_fn):
+//
+//   PH_GRAM  A = X X^T                  symmetric: upper tiles only + mirror
+//   PH_A2B   B = b A + c (A A)          symmetric: upper tiles only + mirror
+//   PH_BX    X' = a X + B X             full tiles, written to the other X buffer
+//
+// One persistent kernel per phase, one CTA per SM, a 128 x 256 output tile per
+// work item, tiles of every shape bucket of the launch in one static schedule.
+// Warp roles (192 threads):
+//   warp 0 lane 0   TMA producer: K-blocks of 64 into a 4-stage smem ring
+//   warp 1          TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=256,
+//                   K=16, bf16 in, fp32 accumulate) and commits to mbarriers
+//   warps 2-5       epilogue: tcgen05.ld of the accumulator (two TMEM buffers
+//                   of 256 columns, so the next tile's MMAs overlap), fused
+//                   scalar epilogue in fp32, bf16 stores
+// Operands: X, A, B are zero-padded in the workspace (rows to 128, cols to
+// 64), so every K-block is full and the MMA needs no masking; tiles that hang
+// over the padded edge read TMA's zero fill and skip their stores.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nsk {
+namespace {
+
+using namespace nsptx;
+
+constexpr int BM = GEMM_BM, BN = GEMM_BN, BK = GEMM_BK, UK = 16;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 256 columns
+constexpr int THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+
+template <int PHASE>
+__device__ __forceinline__ void decode_tile(const GemmParams& p, long long t, int& b, int& mat, int& tm, int& tn) {
+  b = 0;
+  while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
+  const GemmBucket& B = p.bk[b];
+  const long long local = t - B.tile_begin;
+  mat = static_cast<int>(local / B.tiles_per_mat);
+  int r = static_cast<int>(local % B.tiles_per_mat);
+  if (PHASE == PH_BX) {
+    tm = r / B.tiles_n;
+    tn = r % B.tiles_n;
+  } else {
+    // upper-triangle tiles: in tile row tm, column tiles from floor(tm*BM/BN)
+    tm = 0;
+    while (true) {
+      const int tn0 = (tm * BM) / BN;
+      const int cnt = B.tiles_n - tn0;
+      if (r < cnt) {
+        tn = tn0 + r;
+        break;
+      }
+      r -= cnt;
+      ++tm;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& q, float* f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool B_MN = (PHASE == PH_BX);
+  constexpr bool SYRK = (PHASE != PH_BX);
+  constexpr uint32_t IDESC = idesc_make(1u, BM, BN, false, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (blockDim.x != THREADS) {
+    if (threadIdx.x == 0) atomicOr(p.status, NS_DEV_BAD_LAUNCH);
+    return;
+  }
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    for (int b = 0; b < p.nb; ++b) {
+      prefetch_tmap(&p.tma[b]);
+      prefetch_tmap(&p.tmb[b]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    long long issued = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
+        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        uint8_t* a_dst = sA + stage * A_BYTES;
+        uint8_t* b_dst = sB + stage * B_BYTES;
+        tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
+        if (!B_MN) {
+          tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
+          tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    if (*abort_flag) {
+      // let the copies already issued land before the CTA exits
+      const long long first = issued > STAGES ? issued - STAGES : 0;
+      for (long long i = first; i < issued; ++i)
+        mbar_wait_drain(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.status);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ----------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto mma_done;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k) {
+          const uint64_t ad = sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+          const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+                                   : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
+          mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit(&tfull[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  mma_done:
+    if (*abort_flag) {
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.status);
+    }
+  } else if (warp >= 2) {
+    // -------------------------------------------------------------- epilogue
+    const int lg = warp & 3;  // this warp may read TMEM lanes [32*lg, 32*lg + 32)
+    uint32_t acc = 0, acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      const GemmBucket& B = p.bk[b];
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int r0w = tm * BM + lg * 32;  // first row of this warp
+      const int r = r0w + lane;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(mat) * B.out_stride;
+      const __nv_bfloat16* aux =
+          reinterpret_cast<const __nv_bfloat16*>(B.aux) + static_cast<long long>(mat) * B.aux_stride;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int cg = tn * BN + c0;
+        if (cg >= B.cols_valid) break;          // warp-uniform
+        if (SYRK && cg + 31 < r0w) continue;    // chunk entirely below the diagonal for this warp
+        uint32_t v[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + acc * BN + c0, v);
+        tmem_ld_wait();
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (PHASE != PH_GRAM) {
+          const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<long long>(r) * B.ld_aux + cg);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float x[8];
+            unpack_bf16x8(src[q], x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (PHASE == PH_A2B)
+                f[q * 8 + e] = p.beta * x[e] + p.gamma * f[q * 8 + e];
+              else
+                f[q * 8 + e] = p.alpha * x[e] + f[q * 8 + e];
+            }
+          }
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack_bf16(f[2 * j], f[2 * j + 1]);
+        __nv_bfloat16* dst = out + static_cast<long long>(r) * B.ld_out + cg;
+        if (!SYRK || cg >= r) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        } else {
+          // straddles the diagonal: keep the columns c >= r
+          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(w);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (cg + j >= r) dst[j] = hv[j];
+        }
+        if (SYRK) {
+          // mirror the strictly-upper part: element (r, c) also goes to (c, r);
+          // lanes hold consecutive r, so each store instruction is contiguous
+          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(w);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = cg + j;
+            if (c > r) out[static_cast<long long>(c) * B.ld_out + r] = hv[j];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st) {
+  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+  cudaError_t e;
+  switch (phase) {
+    case PH_GRAM:
+      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+      ns_gemm_kernel<PH_GRAM><<<grid, THREADS, SMEM_BYTES, st>>>(p);
+      break;
+    case PH_A2B:
+      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_A2B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+      ns_gemm_kernel<PH_A2B><<<grid, THREADS, SMEM_BYTES, st>>>(p);
+      break;
+    case PH_BX:
+      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_BX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+      ns_gemm_kernel<PH_BX><<<grid, THREADS, SMEM_BYTES, st>>>(p);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nsk

@@ -28,7 +28,7 @@ struct GemmBucket {
   int cols_valid;        // output columns that exist (m_pad or n_pad)
 };
 
-struct alignas(64) GemmParams {
+struct GemmParams {
   CUtensorMap tma[GEMM_MAX_BUCKETS];  // A operand, K-major, box {64, 128, 1}
   CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} / MN-major box {64,64,1}
   GemmBucket bk[GEMM_MAX_BUCKETS];

@@ -1,0 +1,201 @@
+// Memory-bound kernels around the Newton-Schulz products (Megatron-Core API
+// page owner_planning, ns_cost_fn: view as (shape[0], prod(shape[1:])),
+// normalise, transpose so rows <= cols; the result is transposed back).
+//
+//   ns_sumsq_kernel   per-matrix partial sums of squares over 32K-element chunks
+//   ns_scale_kernel   scale = 1 / (sqrt(sum of partials) + eps), fixed order
+//   ns_prep_kernel    X_0 = scale * (T or T^T), zero-padded to m_pad x n_pad, bf16
+//   ns_store_kernel   out = X_k (or X_k^T) cropped to the tensor's (rows, cols)
+//
+// Each launch covers up to PRO_MAX_MATS matrices of one shape bucket; the
+// per-matrix pointers travel in the parameter block.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "status.h"
+
+namespace nsk {
+namespace {
+
+constexpr int SUMSQ_THREADS = 256;
+constexpr long long SUMSQ_CHUNK = 32768;
+constexpr int TILE = 64;
+
+__device__ __forceinline__ float bf16_to_f(unsigned short h) { return __uint_as_float(uint32_t(h) << 16); }
+
+__device__ __forceinline__ float block_sum(float v) {
+  __shared__ float red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = (threadIdx.x < blockDim.x / 32) ? red[threadIdx.x] : 0.0f;
+  if (w == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(SUMSQ_THREADS) ns_sumsq_kernel(const __grid_constant__ ProParams p) {
+  const MatDesc& d = p.md[blockIdx.y];
+  const long long c0 = static_cast<long long>(blockIdx.x) * SUMSQ_CHUNK;
+  if (c0 >= d.numel) return;
+  const long long c1 = min(d.numel, c0 + SUMSQ_CHUNK);
+  const unsigned short* src = reinterpret_cast<const unsigned short*>(d.in);
+  float acc = 0.0f;
+  if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    const long long v0 = c0 / 8, v1 = c1 / 8;  // c0 is a multiple of 8
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (long long i = v0 + threadIdx.x; i < v1; i += blockDim.x) {
+      const uint4 q = __ldg(&s4[i]);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+        acc = fmaf(lo, lo, acc);
+        acc = fmaf(hi, hi, acc);
+      }
+    }
+    for (long long i = v1 * 8 + threadIdx.x; i < c1; i += blockDim.x) {
+      const float x = bf16_to_f(src[i]);
+      acc = fmaf(x, x, acc);
+    }
+  } else {
+    for (long long i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+      const float x = bf16_to_f(src[i]);
+      acc = fmaf(x, x, acc);
+    }
+  }
+  acc = block_sum(acc);
+  if (threadIdx.x == 0) d.partial[blockIdx.x] = acc;
+}
+
+__global__ void __launch_bounds__(256) ns_scale_kernel(const __grid_constant__ ProParams p) {
+  const MatDesc& d = p.md[blockIdx.x];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < p.nchunks; i += blockDim.x) s += static_cast<double>(d.partial[i]);
+  // fixed-order reduction in double
+  __shared__ double red[256];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *d.scale = static_cast<float>(1.0 / (sqrt(red[0]) + static_cast<double>(p.eps)));
+}
+
+// One 64 x 64 tile of X_0 per CTA (blockIdx.x over the padded tile grid,
+// blockIdx.y over matrices). X_0[i][j] = scale * V[i][j] for i < m, j < n,
+// else 0, where V = T (rows <= cols) or T^T (rows > cols).
+__global__ void __launch_bounds__(256) ns_prep_kernel(const __grid_constant__ ProParams p) {
+  __shared__ float tile[TILE][TILE + 1];
+  const MatDesc& d = p.md[blockIdx.y];
+  const int tiles_n = p.n_pad / TILE;
+  const int ti = blockIdx.x / tiles_n, tj = blockIdx.x % tiles_n;
+  const int i0 = ti * TILE, j0 = tj * TILE;
+  const float s = *d.scale;
+  const unsigned short* src = reinterpret_cast<const unsigned short*>(d.in);
+  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(d.x);
+  const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;  // 64 x 4
+  if (!d.transposed) {
+    // V = T, row-major with leading dimension cols = n
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      float v = 0.0f;
+      if (i < p.m && j < p.n) v = s * bf16_to_f(src[static_cast<long long>(i) * p.n + j]);
+      x[static_cast<long long>(i) * p.n_pad + j] = __float2bfloat16_rn(v);
+    }
+  } else {
+    // V = T^T, T row-major (n x m): V[i][j] = T[j][i]; stage T[j0.., i0..] in smem
+    for (int jj = ty; jj < TILE; jj += 4) {
+      const int j = j0 + jj, i = i0 + tx;
+      float v = 0.0f;
+      if (i < p.m && j < p.n) v = s * bf16_to_f(src[static_cast<long long>(j) * p.m + i]);
+      tile[jj][tx] = v;
+    }
+    __syncthreads();
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      x[static_cast<long long>(i) * p.n_pad + j] = __float2bfloat16_rn(tile[tx][ii]);
+    }
+  }
+}
+
+// One 64 x 64 tile of the output (rows x cols) per CTA.
+__global__ void __launch_bounds__(256) ns_store_kernel(const __grid_constant__ ProParams p) {
+  __shared__ float tile[TILE][TILE + 1];
+  const MatDesc& d = p.md[blockIdx.y];
+  const int rows = d.rows, cols = d.cols;
+  const int tiles_c = (cols + TILE - 1) / TILE;
+  const int ti = blockIdx.x / tiles_c, tj = blockIdx.x % tiles_c;
+  const int i0 = ti * TILE, j0 = tj * TILE;
+  const unsigned short* x = reinterpret_cast<const unsigned short*>(d.xfinal);
+  const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;
+  if (!d.transposed) {
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      if (i < rows && j < cols) {
+        const float v = bf16_to_f(x[static_cast<long long>(i) * p.n_pad + j]);
+        if (p.out_f32)
+          reinterpret_cast<float*>(d.out)[static_cast<long long>(i) * cols + j] = v;
+        else
+          reinterpret_cast<__nv_bfloat16*>(d.out)[static_cast<long long>(i) * cols + j] = __float2bfloat16_rn(v);
+      }
+    }
+  } else {
+    // out[i][j] = X[j][i]; X is m_pad x n_pad with j < m (= cols), i < n (= rows)
+    for (int jj = ty; jj < TILE; jj += 4) {
+      const int j = j0 + jj, i = i0 + tx;
+      float v = 0.0f;
+      if (i < rows && j < cols) v = bf16_to_f(x[static_cast<long long>(j) * p.n_pad + i]);
+      tile[jj][tx] = v;
+    }
+    __syncthreads();
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      if (i < rows && j < cols) {
+        const float v = tile[tx][ii];
+        if (p.out_f32)
+          reinterpret_cast<float*>(d.out)[static_cast<long long>(i) * cols + j] = v;
+        else
+          reinterpret_cast<__nv_bfloat16*>(d.out)[static_cast<long long>(i) * cols + j] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0 || p.nchunks <= 0) return cudaSuccess;
+  ns_sumsq_kernel<<<dim3(p.nchunks, p.count), SUMSQ_THREADS, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0) return cudaSuccess;
+  ns_scale_kernel<<<p.count, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0) return cudaSuccess;
+  const int tiles = (p.m_pad / TILE) * (p.n_pad / TILE);
+  ns_prep_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_store(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0) return cudaSuccess;
+  const int rows = p.md[0].rows, cols = p.md[0].cols;
+  // all matrices of a bucket have the same (rows, cols) up to a transpose,
+  // so the tile count is the same for each
+  const int tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
+  ns_store_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nsk

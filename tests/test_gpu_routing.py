@@ -1,0 +1,109 @@
+"""GPU pack (shard -> home) and unpack (home -> shard) against the oracle,
+bit for bit, for the row-shard and flat-buffer models."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import bits
+from oracle import planning as op
+from oracle import routing as orr
+
+pytestmark = pytest.mark.gpu
+nsg = pytest.importorskip("newton_schulz_shape_gb300")
+
+
+def _row_shard_case(shapes, S, shard_dim, seed, home_of=None):
+    dev = torch.device("cuda:0")
+    ts = workloads.gen_tensors(workloads.Workload("route", shapes, 1.0, seed))
+    np_ts = [bits(t).reshape(t.shape) for t in ts]
+    plan = nsg.ns_plan_create(shapes, S=S, shard_dim=shard_dim, home_of=home_of)
+    homes = plan.homes()
+    home_of_d = {i: h for i, h in enumerate(homes)}
+    ranks_np = orr.make_rank_buffers(np_ts, S, shard_dim)
+    want_homes = orr.route_to_ns_home(ranks_np, shapes, home_of_d, S, shard_dim)
+    rank_t = [torch.from_numpy(r.view(np.int16).copy()).view(torch.bfloat16).to(dev) for r in ranks_np]
+    _, hs, _ = plan.home_layout()
+    home_t = [torch.full((max(1, n),), -1.0, dtype=torch.bfloat16, device=dev) for n in hs]
+    nsg.ns_pack_to_home(plan, rank_t, home_t)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for h in range(S):
+        assert np.array_equal(bits(home_t[h])[:hs[h]], want_homes[h])
+    back = [torch.zeros_like(r) for r in rank_t]
+    nsg.ns_unpack_from_home(plan, home_t, back)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for r in range(S):
+        assert np.array_equal(bits(back[r]), ranks_np[r])
+
+
+@pytest.mark.parametrize("S", [1, 2, 8])
+def test_row_shard_dim0(S):
+    shapes = workloads.gen_random_shapes(25, 100 + S, 300, S)
+    _row_shard_case(shapes, S, 0, 21)
+
+
+@pytest.mark.parametrize("S,shard_dim", [(2, 1), (3, 1), (4, 2)])
+def test_row_shard_other_dims(S, shard_dim):
+    shapes = [(5, 12, 7), (3, 24, 4), (2, 36, 8), (6, 12, 4)] if shard_dim == 1 else \
+             [(3, 5, 8, 2), (2, 3, 12, 5), (4, 1, 4, 3)]
+    _row_shard_case(shapes, S, shard_dim, 22)
+
+
+def test_row_shard_empty_homes_and_odd_alignment():
+    # every param homed on rank 2: ranks 0, 1, 3 own nothing; odd element counts
+    shapes = [(4, 3), (8, 5), (4, 7), (12, 1)]
+    _row_shard_case(shapes, 4, 0, 23, home_of=[2, 2, 2, 2])
+
+
+def test_row_shard_large_moe_slice():
+    shapes = [(1408, 2048), (1408, 2048), (2048, 1408)] * 8
+    _row_shard_case(shapes, 8, 0, 24)
+
+
+def _flat_case(shapes, offsets, size, S, seed, owner_of=None):
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(seed)
+    flat = (torch.randn(size, generator=g)).to(torch.bfloat16)
+    flat_np = bits(flat)
+    per = size // S
+    plan = nsg.ns_plan_create_flat(shapes, offsets, size, S=S, owner_of=owner_of)
+    owners = {i: h for i, h in enumerate(plan.homes()) if h >= 0}
+    numels = [int(np.prod(s)) for s in shapes]
+    ranks_np = [flat_np[r * per:(r + 1) * per] for r in range(S)]
+    want = orr.flat_pack_to_owner(ranks_np, offsets, numels, size, S, owners)
+    rank_t = [flat[r * per:(r + 1) * per].clone().to(dev) for r in range(S)]
+    _, hs, _ = plan.home_layout()
+    home_t = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    nsg.ns_pack_to_home(plan, rank_t, home_t)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for h in range(S):
+        assert np.array_equal(bits(home_t[h])[:hs[h]], want[h])
+    # unpack into buffers pre-filled with a marker: non-participating slots keep it
+    marker = [torch.full((per,), 7.0, dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    nsg.ns_unpack_from_home(plan, home_t, marker)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    before = [bits(torch.full((per,), 7.0, dtype=torch.bfloat16)) for _ in range(S)]
+    want_back = orr.flat_unpack_from_owner([bits(h)[:n] for h, n in zip(home_t, hs)], before, offsets,
+                                           numels, size, S, owners)
+    for r in range(S):
+        assert np.array_equal(bits(marker[r]), want_back[r])
+
+
+def test_flat_worked_example_on_gpu():
+    _flat_case([(6, 4), (4, 4)], [0, 24], 40, 2, 31, owner_of=[1, 1])
+    _flat_case([(6, 4), (4, 4)], [0, 24], 40, 2, 32)
+
+
+@pytest.mark.parametrize("S", [2, 3, 5])
+def test_flat_random(S):
+    g = np.random.default_rng(S)
+    shapes, offsets, pos = [], [], 0
+    for _ in range(30):
+        shp = (int(g.integers(1, 40)),) if g.random() < 0.2 else (int(g.integers(1, 60)), int(g.integers(1, 90)))
+        pos += int(g.integers(0, 5))
+        offsets.append(pos)
+        shapes.append(shp)
+        pos += int(np.prod(shp))
+    size = ((pos + S - 1) // S) * S
+    _flat_case(shapes, offsets, size, S, 40 + S)
