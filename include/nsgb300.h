@@ -193,6 +193,22 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
  * NS_ERR_CUDA on a pending CUDA error, else NS_OK. plan may be NULL. */
 int ns_check_status(ns_plan_t* plan, void* stream);
 
+/* ------------------------------------------------------------ measurement
+ * Not part of the pages' interface: support for measuring the kernels above.
+ * Kernel kinds: 0 = Gram (X X^T), 1 = A*A with the b*A + c*A^2 epilogue,
+ * 2 = B*X with the a*X epilogue, 3 = norm/scale/transpose prologue and
+ * output store, 4 = pack/unpack. Launch counters are always on. When timing
+ * is enabled, every launch is bracketed by two CUDA events recorded on the
+ * stream it is launched on; ns_profile_read synchronises those events. */
+
+/* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */
+int ns_profile_enable(int enable);
+
+/* launches[5] (may be NULL) receives the launch count per kind and gpu_ms[5]
+ * (may be NULL) the summed event time per kind since the last reset; reset
+ * != 0 clears both afterwards. */
+int ns_profile_read(int reset, int64_t* launches, double* gpu_ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -199,3 +199,19 @@ def _plan_shard_dim(plan: NsPlan) -> int:
 def ns_check_status(plan: NsPlan = None, stream=None) -> int:
     """Synchronise the stream and return the device status (NS_OK or an error code)."""
     return lib.ns_check_status(plan.handle if plan is not None else None, _stream(stream))
+
+
+KERNEL_KINDS = ("gram", "a2b", "bx", "prologue_store", "pack_unpack")
+
+
+def ns_profile_enable(enable: bool = True) -> None:
+    """Per-launch CUDA-event timing inside the library (measurement only)."""
+    check(lib.ns_profile_enable(1 if enable else 0), "ns_profile_enable")
+
+
+def ns_profile_read(reset: bool = False):
+    """Return ({kind: launches}, {kind: summed gpu ms}) since the last reset."""
+    n = (ctypes.c_int64 * 5)()
+    ms = (ctypes.c_double * 5)()
+    check(lib.ns_profile_read(1 if reset else 0, n, ms), "ns_profile_read")
+    return dict(zip(KERNEL_KINDS, list(n))), dict(zip(KERNEL_KINDS, list(ms)))

@@ -41,6 +41,56 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// ----------------------------------------------------------- measurement
+constexpr int kKinds = 5;
+enum { K_GRAM = 0, K_A2B = 1, K_BX = 2, K_PRO = 3, K_PACK = 4 };
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+long long g_launches[kKinds] = {0};
+double g_ms[kKinds] = {0};
+struct PendingTiming {
+  cudaEvent_t a, b;
+  int kind;
+};
+std::vector<PendingTiming> g_pending;
+std::vector<cudaEvent_t> g_free_events;
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch through `fn`, counting it and, if timing is on, bracketing it with
+// events on `st`.
+template <typename F>
+cudaError_t counted(int kind, cudaStream_t st, F&& fn) {
+  bool timed;
+  cudaEvent_t a = nullptr, b = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ++g_launches[kind];
+    timed = g_prof_on;
+    if (timed) {
+      a = take_event();
+      b = take_event();
+    }
+  }
+  if (timed && a) cudaEventRecord(a, st);
+  cudaError_t e = fn();
+  if (timed && b) {
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_pending.push_back({a, b, kind});
+  }
+  return e;
+}
+
 // Per-device set-up: status word address, SM count, architecture check.
 int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out) {
   int dev = 0;
@@ -183,7 +233,8 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
   gp.nb = nb;
   gp.total_tiles = tiles;
   const int grid = static_cast<int>(std::min<long long>(tiles, nsm));
-  return nsk::launch_gemm(phase, gp, grid, st) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+  return counted(phase, st, [&] { return nsk::launch_gemm(phase, gp, grid, st); }) == cudaSuccess ? NS_OK
+                                                                                           : NS_ERR_CUDA;
 }
 
 int upload_route(Plan& p, int dev) {
@@ -236,7 +287,7 @@ int route(ns_plan_t* plan, void* const* rank_bufs, void* const* home_bufs, int S
   pp.elem_bytes = elem_bytes;
   pp.to_home = to_home ? 1 : 0;
   pp.status = status;
-  return nsk::launch_pack(pp, st) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+  return counted(K_PACK, st, [&] { return nsk::launch_pack(pp, st); }) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
 
 }  // namespace
@@ -296,8 +347,9 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
         d.cols = static_cast<int>(t.cols);
         d.transposed = t.transposed ? 1 : 0;
       }
-      if (nsk::launch_sumsq(pp, st) != cudaSuccess || nsk::launch_scale(pp, st) != cudaSuccess ||
-          nsk::launch_prep(pp, st) != cudaSuccess)
+      if (counted(K_PRO, st, [&] { return nsk::launch_sumsq(pp, st); }) != cudaSuccess ||
+          counted(K_PRO, st, [&] { return nsk::launch_scale(pp, st); }) != cudaSuccess ||
+          counted(K_PRO, st, [&] { return nsk::launch_prep(pp, st); }) != cudaSuccess)
         return NS_ERR_CUDA;
     }
   }
@@ -339,7 +391,7 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
         d.transposed = t.transposed ? 1 : 0;
         d.numel = t.numel;
       }
-      if (nsk::launch_store(pp, st) != cudaSuccess) return NS_ERR_CUDA;
+      if (counted(K_PRO, st, [&] { return nsk::launch_store(pp, st); }) != cudaSuccess) return NS_ERR_CUDA;
     }
   }
   return NS_OK;
@@ -374,6 +426,36 @@ int ns_check_status(ns_plan_t* /*plan*/, void* stream) {
   }
   if (cudaGetLastError() != cudaSuccess) return NS_ERR_CUDA;
   return NS_OK;
+}
+
+int ns_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+  return NS_OK;
+}
+
+int ns_profile_read(int reset, int64_t* launches, double* gpu_ms) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int rc = NS_OK;
+  for (const PendingTiming& t : g_pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(t.b) != cudaSuccess || cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess)
+      rc = NS_ERR_CUDA;
+    else
+      g_ms[t.kind] += ms;
+    g_free_events.push_back(t.a);
+    g_free_events.push_back(t.b);
+  }
+  g_pending.clear();
+  for (int k = 0; k < kKinds; ++k) {
+    if (launches) launches[k] = g_launches[k];
+    if (gpu_ms) gpu_ms[k] = g_ms[k];
+    if (reset) {
+      g_launches[k] = 0;
+      g_ms[k] = 0.0;
+    }
+  }
+  return rc;
 }
 
 int ns_plan_destroy(ns_plan_t* plan) {
