@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Throughput of the shape-batched Newton-Schulz hot path on GB300.
+
+One step = pack (S = 8 simulated row-shard ranks -> LPT homes) -> quintic
+Newton-Schulz on every matrix (5 steps, bf16 path) -> unpack (homes -> ranks),
+all through the C ABI of libnsgb300.so. Default workload: GPT-style 24 layers,
+d = 2048, ffn = 8192 (QKV 6144x2048, O 2048x2048, up 8192x2048,
+down 2048x8192 per layer; 96 matrices, 2.42 GB of bf16 per step).
+
+Prints one JSON line (rank 0). ``value`` is matrices/s with inputs resident in
+HBM; ``e2e`` is the same metric with the host->device copy of the rank shards
+and the device->host copy of the results inside the timed region.
+``--impl reference`` times the float64 CPU oracle instead, on a bounded
+sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
+scaling, no data-path collective); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NS matrices/s and achieved TFLOP/s vs GB300 dense bf16 peak (1 GPU)"
+UNIT = "matrices/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe"], default="gpt")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def get_workload(name: str):
+    import workloads
+    return {"gpt": workloads.gpt_24l_d2048, "small": workloads.small_16x128x256,
+            "llama": workloads.llama8b_32l, "moe": workloads.moe_16l_64e}[name]()
+
+
+def view_mn(shape):
+    rows = shape[0]
+    cols = 1
+    for d in shape[1:]:
+        cols *= d
+    return min(rows, cols), max(rows, cols)
+
+
+def flops_by_kind(shapes, k):
+    """Algorithmic flops per call by kernel kind: Gram 2 m^2 n, A*A 2 m^3,
+    B*X 2 m^2 n per matrix per step (useful total k (4 m^2 n + 2 m^3))."""
+    g = a2 = bx = 0
+    for s in shapes:
+        m, n = view_mn(s)
+        g += 2 * m * m * n * k
+        a2 += 2 * m * m * m * k
+        bx += 2 * m * m * n * k
+    return {"gram": g, "a2b": a2, "bx": bx}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def traffic_for(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    src = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc", "gemm.cu")
+    summ = os.path.join(ROOT, "profiles", "gemm_traffic.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(summ):
+            if line.startswith("traffic:"):
+                kv = dict(x.strip().split("=", 1) for x in line[len("traffic:"):].split(";") if "=" in x)
+                if kv.get("kernel") == kernel and kv.get("gemm_cu_sha256") == sha:
+                    return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nsgb300_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(w, budget_s: float = 20.0):
+    """Time the float64 oracle on one matrix per shape bucket (and the routing
+    oracle on those tensors), extrapolated to the whole workload by count."""
+    import numpy as np
+    import workloads
+    from oracle import ns as ons
+    from oracle import routing as orr
+    buckets = {}
+    for i, s in enumerate(w.shapes):
+        buckets.setdefault(view_mn(s), []).append(i)
+    total_est = 0.0
+    sample = []
+    spent = 0.0
+    for (m, n), idx in buckets.items():
+        i = idx[0]
+        t = workloads.gen_tensor(w.shapes[i], w.sigma, w.seed, i)
+        x = t.float().numpy()
+        bits = t.view(__import__("torch").int16).numpy()
+        t0 = time.perf_counter()
+        ons.newton_schulz(x, workloads.STEPS, workloads.A_COEF, workloads.B_COEF, workloads.C_COEF, workloads.EPS)
+        ranks = orr.make_rank_buffers([bits], w.S, 0)
+        homes = orr.route_to_ns_home(ranks, [w.shapes[i]], {0: 0}, w.S, 0)
+        orr.route_from_ns_home(homes, [w.shapes[i]], {0: 0}, w.S, 0)
+        dt = time.perf_counter() - t0
+        spent += dt
+        total_est += dt * len(idx)
+        sample.append(f"{len(idx)}x{tuple(w.shapes[i])}: {dt:.2f}s")
+        if spent > budget_s:
+            break
+    try:
+        import threadpoolctl
+        threads = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
+    except Exception:
+        threads = os.cpu_count()
+    return len(w.shapes) / total_est, threads, "one matrix per (m, n) bucket, NS + pack/unpack oracle, " \
+        "extrapolated by bucket count: " + "; ".join(sample)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = get_workload(args.workload)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, threads, sample = cpu_oracle_sample(w)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * len(w.shapes) / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "matrices": len(w.shapes), "S": w.S},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our path
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import newton_schulz_shape_gb300 as nsg
+    import workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = get_workload(args.workload)
+    if world > 1:
+        w.seed += 7919 * rank      # each rank: its own replica of the workload
+    S, shapes = w.S, w.shapes
+    plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=S, shard_dim=0)
+    home_off, home_sizes, rank_sizes = plan.home_layout()
+    homes = plan.homes()
+    L = rank_sizes[0]
+
+    # host inputs: rank r's shards of every tensor, in index order (pinned)
+    rank_host = [torch.empty(L, dtype=torch.bfloat16, pin_memory=True) for _ in range(S)]
+    pos = 0
+    for i, s in enumerate(shapes):
+        t = workloads.gen_tensor(s, w.sigma, w.seed, i).reshape(S, -1)
+        n = t.shape[1]
+        for r in range(S):
+            rank_host[r][pos:pos + n].copy_(t[r])
+        pos += n
+    out_host = [torch.empty(L, dtype=torch.bfloat16, pin_memory=True) for _ in range(S)]
+
+    rank_in = [h.to(dev) for h in rank_host]
+    home_in = [torch.empty(max(1, n), dtype=torch.bfloat16, device=dev) for n in home_sizes]
+    home_out = [torch.empty(max(1, n), dtype=torch.bfloat16, device=dev) for n in home_sizes]
+    rank_out = [torch.empty(L, dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ins = [home_in[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
+    outs = [home_out[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        nsg.ns_unpack_from_home(plan, home_out, rank_out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    rc = nsg.ns_check_status(plan, stream)
+    if rc != nsg.NS_OK:
+        raise RuntimeError(f"device status after warm-up: {nsg.ns_status_string(rc)}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    uuid = ""
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+
+    # ---- device-resident timed region (per-phase events on the launch stream)
+    nsg.ns_profile_read(reset=True)
+    nsg.ns_profile_enable(True)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
+        ev[k][1].record(stream)
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        ev[k][2].record(stream)
+        nsg.ns_unpack_from_home(plan, home_out, rank_out, stream=stream)
+        ev[k][3].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    nsg.ns_profile_enable(False)
+    launches, kms = nsg.ns_profile_read(reset=True)
+    rc = nsg.ns_check_status(plan, stream)
+    if rc != nsg.NS_OK:
+        raise RuntimeError(f"device status after timing: {nsg.ns_status_string(rc)}")
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    pack_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    ns_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    unpack_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    n_mats = len(shapes)
+    value = n_mats * world * 1000.0 / ms_step
+
+    # ---- end to end: H2D of the rank shards, the step, D2H of the results
+    e2e = None
+    if not args.no_e2e:
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for r in range(S):
+                rank_in[r].copy_(rank_host[r], non_blocking=True)
+            step()
+            for r in range(S):
+                out_host[r].copy_(rank_out[r], non_blocking=True)
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        nbytes = 2 * S * L
+        e2e = {"value": n_mats * world * 1000.0 / ms_e2e, "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+    # ---- roofline of the dominant kernel
+    burst, sustained, hbm, peak_src = peaks()
+    fl = flops_by_kind(shapes, workloads.STEPS)
+    gemm_kinds = ["gram", "a2b", "bx"]
+    dom = max(gemm_kinds, key=lambda k: kms.get(k, 0.0))
+    per_launch_ms = kms[dom] / max(1, launches[dom])
+    launches_per_step = launches[dom] / args.steps
+    flops_per_launch = fl[dom] / launches_per_step
+    achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
+    useful = sum(fl.values())
+    roofline = {"bound": "tensor", "kernel": f"ns_gemm_kernel<{dom}>", "achieved": achieved, "peak": sustained,
+                "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": traffic_for(dom),
+                "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); burst {burst}",
+                "flops_per_launch": flops_per_launch, "avg_launch_ms": per_launch_ms}
+    per_kernel = {k: {"launches_per_step": launches[k] / args.steps, "ms_per_step": kms[k] / args.steps}
+                  for k in launches}
+    for k in gemm_kinds:
+        if kms[k] > 0:
+            per_kernel[k]["tflops"] = fl[k] / (kms[k] / args.steps * 1e-3) / 1e12
+    pack_bytes = 2 * 2 * S * L   # read + write, bf16
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0, sigma) bf16 per tensor (sigma 0.02)",
+        "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
+                               f"pack -> NS (5 steps) -> unpack",
+                   "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS,
+                   "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
+        "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
+        "ns_only": {"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,
+                    "frac_of_burst_peak": useful / (ns_ms * 1e-3) / 1e12 / burst},
+        "phases_ms": {"pack": pack_ms, "ns": ns_ms, "unpack": unpack_ms},
+        "pack_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9, "unpack_gbs": pack_bytes / (unpack_ms * 1e-3) / 1e9,
+        "per_kernel": per_kernel,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": int(sum(launches.values())),
+        "roofline": roofline,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, sample = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
