@@ -193,6 +193,23 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
  * NS_ERR_CUDA on a pending CUDA error, else NS_OK. plan may be NULL. */
 int ns_check_status(ns_plan_t* plan, void* stream);
 
+/* No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory when they orthogonalise (e.g. a plugin inside a host program
+ * whose caching allocator owns the GPU's memory, or code that must not call
+ * cudaMalloc after start-up). Same computation and arguments as
+ * ns_orthogonalize_batched, but the scratch memory is a static device array
+ * of NS_FIXED_WS_BYTES inside the library instead of a caller workspace.
+ * Allocates nothing (no cudaMalloc, no cudaFree). Returns NS_ERR_WORKSPACE if
+ * the plan needs more than NS_FIXED_WS_BYTES (see ns_plan_workspace_bytes).
+ * The array exists once per GPU that loads the library and is held until the
+ * process exits. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. Every call shares the array, so calls that
+ * overlap on the GPU (e.g. on two streams) race. */
+#define NS_FIXED_WS_BYTES (64ull << 20)
+int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, void* const* out, int n,
+                                      void* stream);
+
 /* ------------------------------------------------------------ measurement
  * Not part of the pages' interface: support for measuring the kernels above.
  * Kernel kinds: 0 = Gram (X X^T), 1 = A*A with the b*A + c*A^2 epilogue,

@@ -178,6 +178,22 @@ def ns_orthogonalize_batched(plan: NsPlan, ins, outs, workspace, workspace_bytes
                                        int(workspace_bytes), _stream(stream)), "ns_orthogonalize_batched")
 
 
+NS_FIXED_WS_BYTES = 64 << 20
+
+
+def ns_orthogonalize_batched_fixed_ws(plan: NsPlan, ins, outs, stream=None) -> None:
+    """Same as ns_orthogonalize_batched, for callers that cannot allocate a
+    workspace: the library's static scratch array of NS_FIXED_WS_BYTES is used
+    instead. Plans needing more raise NS_ERR_WORKSPACE; calls that overlap on
+    the GPU share that array and race."""
+    n = len(ins)
+    if len(outs) != n:
+        raise ValueError("ins and outs differ in length")
+    check(lib.ns_orthogonalize_batched_fixed_ws(plan.handle, ptr_array([_addr(t) for t in ins]),
+                                                ptr_array([_addr(t) for t in outs]), n, _stream(stream)),
+          "ns_orthogonalize_batched_fixed_ws")
+
+
 def ns_pack_to_home(plan: NsPlan, rank_bufs, home_bufs, shard_dim=None, stream=None) -> None:
     """route_to_ns_home / OwnerGatherPlan: S rank buffers -> S home buffers."""
     sd = 0 if plan.layout == NS_LAYOUT_FLAT else (shard_dim if shard_dim is not None else _plan_shard_dim(plan))
