@@ -42,15 +42,24 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe"], default="gpt")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
 
-def get_workload(name: str):
+PER_LAYER = {"gpt": 4, "llama": 5, "moe": 3 * 64, "small": 1}
+
+
+def get_workload(name: str, layers: int = 0):
     import workloads
-    return {"gpt": workloads.gpt_24l_d2048, "small": workloads.small_16x128x256,
-            "llama": workloads.llama8b_32l, "moe": workloads.moe_16l_64e}[name]()
+    w = {"gpt": workloads.gpt_24l_d2048, "small": workloads.small_16x128x256,
+         "llama": workloads.llama8b_32l, "moe": workloads.moe_16l_64e}[name]()
+    if layers > 0:
+        w.shapes = w.shapes[:layers * PER_LAYER[name]]
+        w.name += f" (first {layers} layers)"
+    return w
 
 
 def view_mn(shape):
@@ -192,7 +201,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = get_workload(args.workload)
+    w = get_workload(args.workload, args.layers)
     for _ in range(args.warmup):
         cpu_oracle_sample(w)
     vals = []
@@ -229,7 +238,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    w = get_workload(args.workload)
+    w = get_workload(args.workload, args.layers)
     if world > 1:
         w.seed += 7919 * rank      # each rank: its own replica of the workload
     S, shapes = w.S, w.shapes

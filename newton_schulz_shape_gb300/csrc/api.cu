@@ -4,7 +4,7 @@
 // ns_orthogonalize_batched follows the Megatron-Core API page owner_planning
 // (ns_cost_fn: view, normalise, transpose so rows <= cols, then per step
 // A = X X^T; X = a X + (b A + c A A) X) and the Megatron-LM issue #6720
-// ("shape-batched NS", "SYRK symmetric kernels"): tensors of equal (m, n)
+// (NS batched by shape, symmetric SYRK-style Gram kernels): tensors of equal (m, n)
 // form a bucket laid out as one [count, m_pad, n_pad] array in the caller's
 // workspace, and every phase of every step runs as one persistent launch over
 // the tiles of all buckets. Nothing here allocates device memory; all

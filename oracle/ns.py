@@ -19,7 +19,7 @@ Readings where the page is silent (each is listed in the design notes):
 * the result is transposed back and reshaped to the input's shape, because
   ``route_from_ns_home`` (page ``core.optimizer.layer_sharded_a2a``) hands
   out (P/S, Q) shards of a (P, Q) result;
-* optional trace ridge (issue #6720, "fp32/TF32 Gram + trace ridge"):
+* optional trace ridge (issue #6720 pairs an fp32/TF32 Gram with a trace ridge):
   A <- A + ridge * (trace(A) / m) * I before B is formed. ``ridge > 0`` is
   parity unpinned: the issue names the ridge but not its form.
 

@@ -15,7 +15,7 @@ Sources
 Readings where the pages are silent:
 
 * costs are exact integers (``ns_cost_fn`` is documented to return an int);
-* "Ties follow buffer order" applies both to equal costs (stable order by
+* the buffer-order tie rule applies both to equal costs (stable order by
   tensor index, tensors being in buffer order) and to equally loaded holders
   (the earliest candidate in buffer order, i.e. the lowest rank);
 * single-candidate tensors are taken in tensor-index order and their cost

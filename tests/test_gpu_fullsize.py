@@ -1,0 +1,121 @@
+"""Parity at full workload sizes, in the launch configuration bench.py times.
+
+The whole workload runs as pack (S = 8 row shards -> LPT homes) -> shape-
+batched Newton-Schulz -> unpack. The float64 oracle then checks sampled
+matrices (one per (m, n) bucket, first and last tensor):
+  * pack: the home buffer holds the complete tensor, bit for bit;
+  * NS: per-matrix relative Frobenius error <= 3e-2;
+  * unpack: every rank buffer holds its shard of the result, bit for bit.
+Every matrix is also checked for properties that hold at any size: finite,
+and ||Y||_F / sqrt(m) inside the band the 5-step map allows for these inputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import BF16_TOL, bits, oracle_ns, rel_err
+
+pytestmark = pytest.mark.gpu
+nsg = pytest.importorskip("newton_schulz_shape_gb300")
+
+
+def view_mn(s):
+    c = int(np.prod(s[1:]))
+    return min(s[0], c), max(s[0], c)
+
+
+def run_pipeline(w, sample=None):
+    dev = torch.device("cuda:0")
+    S, shapes = w.S, w.shapes
+    plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=S, shard_dim=0)
+    home_off, home_sizes, rank_sizes = plan.home_layout()
+    homes = plan.homes()
+    L = rank_sizes[0]
+    if sample is None:
+        seen, sample = set(), [0, len(shapes) - 1]
+        for i, s in enumerate(shapes):
+            if view_mn(s) not in seen:
+                seen.add(view_mn(s))
+                sample.append(i)
+        sample = sorted(set(sample))
+    rank_in = [torch.empty(L, dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    rank_off, kept, pos = [], {}, 0
+    for i, s in enumerate(shapes):
+        t = workloads.gen_tensor(s, w.sigma, w.seed, i)
+        if i in sample:
+            kept[i] = t
+        n = t.numel() // S
+        sh = t.reshape(S, n).to(dev)
+        for r in range(S):
+            rank_in[r][pos:pos + n].copy_(sh[r])
+        rank_off.append(pos)
+        pos += n
+    home_in = [torch.empty(max(1, n), dtype=torch.bfloat16, device=dev) for n in home_sizes]
+    home_out = [torch.empty(max(1, n), dtype=torch.bfloat16, device=dev) for n in home_sizes]
+    rank_out = [torch.empty(L, dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ins = [home_in[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
+    outs = [home_out[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
+    nsg.ns_pack_to_home(plan, rank_in, home_in)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    nsg.ns_unpack_from_home(plan, home_out, rank_out)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    del ws
+
+    # properties of every matrix
+    for i, s in enumerate(shapes):
+        n_el = int(np.prod(s))
+        y = home_out[homes[i]][home_off[i]:home_off[i] + n_el].float()
+        assert torch.isfinite(y).all(), i
+        m, _ = view_mn(s)
+        f = float(torch.linalg.vector_norm(y)) / np.sqrt(m)
+        assert 0.5 < f < 1.2, (i, s, f)
+
+    # sampled matrices against the oracle
+    for i in sample:
+        s = shapes[i]
+        t = kept[i]
+        n_el = t.numel()
+        h = homes[i]
+        got_in = home_in[h][home_off[i]:home_off[i] + n_el]
+        assert np.array_equal(bits(got_in), bits(t).reshape(-1)), ("pack", i)
+        y = home_out[h][home_off[i]:home_off[i] + n_el]
+        err = rel_err(y.reshape(s), oracle_ns(t))
+        assert err <= BF16_TOL, ("ns", i, s, err)
+        ysh = bits(y).reshape(S, -1)
+        for r in range(S):
+            got = bits(rank_out[r][rank_off[i]:rank_off[i] + n_el // S])
+            assert np.array_equal(got, ysh[r]), ("unpack", i, r)
+    return plan
+
+
+def test_gpt_24l_d2048_full():
+    run_pipeline(workloads.gpt_24l_d2048())
+
+
+def test_llama8b_32l_full():
+    run_pipeline(workloads.llama8b_32l())
+
+
+def test_moe_full_size_matrices_two_layers():
+    w = workloads.moe_16l_64e()
+    w.shapes = w.shapes[:2 * 64 * 3]          # 384 matrices at the workload's full per-matrix size
+    run_pipeline(w, sample=[0, 1, 2, 191, 383])
+
+
+@pytest.mark.parametrize("m,aspect", [(1024, 1), (1024, 8), (2048, 2), (4096, 4)])
+def test_sweep_points(m, aspect):
+    w = workloads.sweep_shapes(m, aspect, 2)
+    w.shapes = [w.shapes[0], (aspect * m, m)]   # one wide, one tall (exercises the transpose back)
+    run_pipeline(w, sample=[0, 1])
+
+
+def test_sweep_conv_3d():
+    run_pipeline(workloads.conv_3d(), sample=[0, 31, 63])
+
+
+def test_sweep_8192_square():
+    w = workloads.sweep_shapes(8192, 1, 1)
+    run_pipeline(w, sample=[0])
