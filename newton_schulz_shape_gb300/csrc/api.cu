@@ -169,18 +169,20 @@ BucketPtrs bucket_ptrs(const Bucket& b, char* ws) {
   return q;
 }
 
-// One launch of `phase` over buckets [b0, b1). `cur_is_x0` selects the X buffer
-// the step reads.
-int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
-              unsigned int* status, cudaStream_t st) {
-  nsk::GemmParams gp;
+// Fill the launch parameters of `phase` for buckets [b0, b1). `cur_is_x0`
+// selects the X buffer the step reads. With `final_out` (B*X phase of the
+// last step), every matrix's result goes straight to out[ordinal]: the table
+// entry is the output address with bit 0 set for transposed tensors.
+template <typename P>
+int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1,
+               unsigned int* status, void* const* final_out) {
   std::memset(&gp, 0, sizeof(gp));
   gp.alpha = p.a;
   gp.beta = p.b;
   gp.gamma = p.c;
   gp.status = status;
   long long tiles = 0;
-  int nb = 0;
+  int nb = 0, n_out = 0;
   for (size_t bi = b0; bi < b1; ++bi, ++nb) {
     const Bucket& b = p.buckets[bi];
     const BucketPtrs q = bucket_ptrs(b, ws);
@@ -191,6 +193,8 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
     g.tile_begin = tiles;
     g.count = static_cast<int>(cnt);
     g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
+    g.m_valid = static_cast<int>(b.m);
+    g.n_valid = static_cast<int>(b.n);
     int rc = NS_OK;
     if (phase == nsk::PH_GRAM || phase == nsk::PH_A2B) {
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
@@ -226,15 +230,49 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
       g.aux_stride = b.m_pad * b.n_pad;
       rc = make_map(&gp.tma[nb], q.b, b.m_pad, b.m_pad, cnt, 64, 128);
       if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 64);
+      if (final_out) {
+        g.out_first = n_out;
+        for (size_t s = 0; s < cnt; ++s) {
+          const Tensor& t = p.t[b.members[s]];
+          const unsigned long long a = reinterpret_cast<unsigned long long>(final_out[t.ordinal]);
+          gp.out_tab[n_out++] = a | (t.transposed ? 1ull : 0ull);
+        }
+      }
     }
     if (rc != NS_OK) return rc;
     tiles += static_cast<long long>(g.tiles_per_mat) * static_cast<long long>(cnt);
   }
   gp.nb = nb;
   gp.total_tiles = tiles;
-  const int grid = static_cast<int>(std::min<long long>(tiles, nsm));
+  return NS_OK;
+}
+
+int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
+              unsigned int* status, cudaStream_t st) {
+  nsk::GemmParams gp;
+  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr);
+  if (rc != NS_OK) return rc;
+  const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
   return counted(phase, st, [&] { return nsk::launch_gemm(phase, gp, grid, st); }) == cudaSuccess ? NS_OK
                                                                                            : NS_ERR_CUDA;
+}
+
+// B*X phase of the last step, storing results directly into `out`.
+int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
+                 void* const* out, cudaStream_t st) {
+  static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
+  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out);
+  if (rc != NS_OK) return rc;
+  const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
+  return counted(nsk::PH_BX, st, [&] { return nsk::launch_gemm_final(gp, grid, st); }) == cudaSuccess
+             ? NS_OK
+             : NS_ERR_CUDA;
+}
+
+size_t group_matrices(const Plan& p, size_t b0, size_t b1) {
+  size_t n = 0;
+  for (size_t bi = b0; bi < b1; ++bi) n += p.buckets[bi].members.size();
+  return n;
 }
 
 int upload_route(Plan& p, int dev) {
@@ -353,20 +391,31 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
         return NS_ERR_CUDA;
     }
   }
-  // k steps x (Gram, A*A + B, B*X) over all buckets
+  // k steps x (Gram, A*A + B, B*X) over all buckets. The last B*X launch of
+  // a bucket group writes the results straight to `out` when its per-matrix
+  // table fits the parameter block; other groups go through the store kernel.
+  std::vector<char> stored(p.buckets.size(), 0);
   bool cur_is_x0 = true;
   for (int step = 0; step < p.steps; ++step) {
+    const bool last = step + 1 == p.steps;
     for (int phase = nsk::PH_GRAM; phase <= nsk::PH_BX; ++phase) {
       for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
         const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
-        rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, st);
+        if (last && phase == nsk::PH_BX && group_matrices(p, b0, b1) <= size_t(nsk::GEMM_MAX_OUT)) {
+          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, st);
+          for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
+        } else {
+          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, st);
+        }
         if (rc != NS_OK) return rc;
       }
     }
     cur_is_x0 = !cur_is_x0;
   }
-  // transpose back and store
-  for (const Bucket& b : p.buckets) {
+  // transpose back and store (buckets not stored by the last B*X launch)
+  for (size_t bi = 0; bi < p.buckets.size(); ++bi) {
+    if (stored[bi]) continue;
+    const Bucket& b = p.buckets[bi];
     const BucketPtrs q = bucket_ptrs(b, ws);
     const char* xf = cur_is_x0 ? q.x0 : q.x1;
     const size_t cnt = b.members.size();

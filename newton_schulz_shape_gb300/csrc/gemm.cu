@@ -36,8 +36,8 @@ constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 
 constexpr int THREADS = 192;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
 
-template <int PHASE>
-__device__ __forceinline__ void decode_tile(const GemmParams& p, long long t, int& b, int& mat, int& tm, int& tn) {
+template <int PHASE, typename P>
+__device__ __forceinline__ void decode_tile(const P& p, long long t, int& b, int& mat, int& tm, int& tn) {
   b = 0;
   while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
   const GemmBucket& B = p.bk[b];
@@ -77,8 +77,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& q, float* f) {
   }
 }
 
-template <int PHASE>
-__global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+// FINAL (B*X phase only): write the cropped, transposed-back result to the
+// caller's tensors listed in p.out_tab instead of the next X buffer.
+template <int PHASE, bool FINAL, typename P>
+__global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ P p) {
+  static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
   constexpr bool B_MN = (PHASE == PH_BX);
   constexpr bool SYRK = (PHASE != PH_BX);
   constexpr uint32_t IDESC = idesc_make(1u, BM, BN, false, B_MN);
@@ -245,6 +248,33 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) w[j] = pack_bf16(f[2 * j], f[2 * j + 1]);
+        if (FINAL) {
+          // row r of X_k (m index), columns cg.. (n index) -> the caller's tensor
+          if (r < B.m_valid) {
+            const unsigned long long e = p.out_tab[B.out_first + mat];
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e & ~1ull);
+            const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(w);
+            if (!(e & 1ull)) {
+              __nv_bfloat16* dst = o + static_cast<long long>(r) * B.n_valid + cg;
+              if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.n_valid) dst[j] = hv[j];
+              }
+            } else {
+              // transposed tensor: element (r, c) of X_k is element (c, r) of the
+              // output; lanes hold consecutive r, so each store is contiguous
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (cg + j < B.n_valid) o[static_cast<long long>(cg + j) * B.m_valid + r] = hv[j];
+            }
+          }
+          continue;
+        }
         __nv_bfloat16* dst = out + static_cast<long long>(r) * B.ld_out + cg;
         if (!SYRK || cg >= r) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -285,34 +315,30 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   }
 }
 
+template <int PHASE, bool FINAL, typename P>
+cudaError_t launch_one(const P& p, int grid, cudaStream_t st) {
+  auto kern = ns_gemm_kernel<PHASE, FINAL, P>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st) {
   if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-  cudaError_t e;
   switch (phase) {
-    case PH_GRAM:
-      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_BYTES));
-      if (e != cudaSuccess) return e;
-      ns_gemm_kernel<PH_GRAM><<<grid, THREADS, SMEM_BYTES, st>>>(p);
-      break;
-    case PH_A2B:
-      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_A2B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_BYTES));
-      if (e != cudaSuccess) return e;
-      ns_gemm_kernel<PH_A2B><<<grid, THREADS, SMEM_BYTES, st>>>(p);
-      break;
-    case PH_BX:
-      e = cudaFuncSetAttribute(ns_gemm_kernel<PH_BX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_BYTES));
-      if (e != cudaSuccess) return e;
-      ns_gemm_kernel<PH_BX><<<grid, THREADS, SMEM_BYTES, st>>>(p);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+    case PH_GRAM: return launch_one<PH_GRAM, false>(p, grid, st);
+    case PH_A2B: return launch_one<PH_A2B, false>(p, grid, st);
+    case PH_BX: return launch_one<PH_BX, false>(p, grid, st);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_final(const GemmFinalParams& p, int grid, cudaStream_t st) {
+  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+  return launch_one<PH_BX, true>(p, grid, st);
 }
 
 }  // namespace nsk

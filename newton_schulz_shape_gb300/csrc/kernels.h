@@ -26,9 +26,17 @@ struct GemmBucket {
   int k_blocks;          // K / 64
   int ld_out, ld_aux;    // leading dimensions (elements)
   int cols_valid;        // output columns that exist (m_pad or n_pad)
+  int m_valid, n_valid;  // unpadded m, n (final-store launches)
+  int out_first;         // first entry of this bucket in out_tab (final-store launches)
 };
 
-struct GemmParams {
+// Final-store launches of the B*X phase write each result straight to the
+// caller's output tensor; out_tab holds one entry per matrix: the output
+// address with bit 0 set when the tensor was transposed (rows > cols).
+constexpr int GEMM_MAX_OUT = 3584;
+
+template <int NOUT>
+struct GemmParamsT {
   CUtensorMap tma[GEMM_MAX_BUCKETS];  // A operand, K-major, box {64, 128, 1}
   CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} / MN-major box {64,64,1}
   GemmBucket bk[GEMM_MAX_BUCKETS];
@@ -36,7 +44,11 @@ struct GemmParams {
   int nb;
   float alpha, beta, gamma;  // a, b, c of the quintic step
   unsigned int* status;
+  unsigned long long out_tab[NOUT];
 };
+using GemmParams = GemmParamsT<1>;
+using GemmFinalParams = GemmParamsT<GEMM_MAX_OUT>;
+static_assert(sizeof(GemmFinalParams) <= 32764, "kernel parameter block too large");
 
 constexpr int GEMM_BM = 128, GEMM_BN = 256, GEMM_BK = 64;
 
@@ -95,6 +107,7 @@ struct PackParams {
 
 // ----------------------------------------------------------------- launchers
 cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_final(const GemmFinalParams& p, int grid, cudaStream_t st);
 cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st);
 cudaError_t launch_scale(const ProParams& p, cudaStream_t st);
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st);

@@ -87,39 +87,84 @@ __global__ void __launch_bounds__(256) ns_scale_kernel(const __grid_constant__ P
   if (threadIdx.x == 0) *d.scale = static_cast<float>(1.0 / (sqrt(red[0]) + static_cast<double>(p.eps)));
 }
 
-// One 64 x 64 tile of X_0 per CTA (blockIdx.x over the padded tile grid,
-// blockIdx.y over matrices). X_0[i][j] = scale * V[i][j] for i < m, j < n,
-// else 0, where V = T (rows <= cols) or T^T (rows > cols).
+// X_0 = scale * V zero-padded to m_pad x n_pad, V = T (rows <= cols) or T^T.
+// Non-transposed: each thread writes 16 bytes (8 bf16) of X_0 per iteration,
+// reading T with 16-byte loads when its rows are 16-byte aligned.
+// Transposed: one 64 x 64 tile per CTA through a conflict-free fp32 tile in
+// shared memory, 16-byte loads of T rows and 16-byte stores of X_0 rows.
+// blockIdx.y selects the matrix.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 __global__ void __launch_bounds__(256) ns_prep_kernel(const __grid_constant__ ProParams p) {
-  __shared__ float tile[TILE][TILE + 1];
   const MatDesc& d = p.md[blockIdx.y];
-  const int tiles_n = p.n_pad / TILE;
-  const int ti = blockIdx.x / tiles_n, tj = blockIdx.x % tiles_n;
-  const int i0 = ti * TILE, j0 = tj * TILE;
   const float s = *d.scale;
   const unsigned short* src = reinterpret_cast<const unsigned short*>(d.in);
-  __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(d.x);
-  const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;  // 64 x 4
+  uint4* x4 = reinterpret_cast<uint4*>(d.x);
+  const int nv = p.n_pad / 8;  // 16-byte vectors per X_0 row
   if (!d.transposed) {
-    // V = T, row-major with leading dimension cols = n
-    for (int ii = ty; ii < TILE; ii += 4) {
-      const int i = i0 + ii, j = j0 + tx;
-      float v = 0.0f;
-      if (i < p.m && j < p.n) v = s * bf16_to_f(src[static_cast<long long>(i) * p.n + j]);
-      x[static_cast<long long>(i) * p.n_pad + j] = __float2bfloat16_rn(v);
+    const bool vec = (p.n % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+    const long long total = static_cast<long long>(p.m_pad) * nv;
+    for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+         v += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const int i = static_cast<int>(v / nv);
+      const int j0 = static_cast<int>(v % nv) * 8;
+      float f[8];
+      if (i < p.m && vec && j0 + 8 <= p.n) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(i) * p.n + j0));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[2 * k] = __uint_as_float(w[k] << 16);
+          f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          f[k] = (i < p.m && j0 + k < p.n) ? bf16_to_f(src[static_cast<long long>(i) * p.n + j0 + k]) : 0.0f;
+      }
+      x4[v] = make_uint4(pack2(s * f[0], s * f[1]), pack2(s * f[2], s * f[3]), pack2(s * f[4], s * f[5]),
+                         pack2(s * f[6], s * f[7]));
     }
   } else {
-    // V = T^T, T row-major (n x m): V[i][j] = T[j][i]; stage T[j0.., i0..] in smem
-    for (int jj = ty; jj < TILE; jj += 4) {
-      const int j = j0 + jj, i = i0 + tx;
-      float v = 0.0f;
-      if (i < p.m && j < p.n) v = s * bf16_to_f(src[static_cast<long long>(j) * p.m + i]);
-      tile[jj][tx] = v;
+    // V[i][j] = T[j][i], T row-major n x m. Tile (ti, tj) of X_0.
+    __shared__ float tile[TILE][TILE + 1];
+    const int tiles_n = p.n_pad / TILE;
+    const int ti = blockIdx.x / tiles_n, tj = blockIdx.x % tiles_n;
+    const int i0 = ti * TILE, j0 = tj * TILE;
+    const bool vec = (p.m % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+    // load: 64 rows j of T x 8 vectors of 8 i each; 512 vectors, 2 per thread
+    for (int e = threadIdx.x; e < TILE * 8; e += blockDim.x) {
+      const int jj = e / 8, iv = (e % 8) * 8;
+      const int j = j0 + jj, i = i0 + iv;
+      float f[8];
+      if (j < p.n && vec && i + 8 <= p.m) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(j) * p.m + i));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[2 * k] = __uint_as_float(w[k] << 16);
+          f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          f[k] = (j < p.n && i + k < p.m) ? bf16_to_f(src[static_cast<long long>(j) * p.m + i + k]) : 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tile[jj][iv + k] = f[k];
     }
     __syncthreads();
-    for (int ii = ty; ii < TILE; ii += 4) {
-      const int i = i0 + ii, j = j0 + tx;
-      x[static_cast<long long>(i) * p.n_pad + j] = __float2bfloat16_rn(tile[tx][ii]);
+    // store: 64 rows i of X_0 x 8 vectors of 8 j
+    for (int e = threadIdx.x; e < TILE * 8; e += blockDim.x) {
+      const int ii = e % TILE, jv = (e / TILE) * 8;
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = s * tile[jv + k][ii];
+      x4[(static_cast<long long>(i0 + ii) * p.n_pad + j0 + jv) / 8] =
+          make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
     }
   }
 }
@@ -183,6 +228,8 @@ cudaError_t launch_scale(const ProParams& p, cudaStream_t st) {
 
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
+  // one CTA per 64 x 64 tile (the transposed path needs exactly that grid; the
+  // plain path grid-strides over the same number of CTAs)
   const int tiles = (p.m_pad / TILE) * (p.n_pad / TILE);
   ns_prep_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
   return cudaGetLastError();
