@@ -328,6 +328,246 @@ int route(ns_plan_t* plan, void* const* rank_bufs, void* const* home_bufs, int S
   return counted(K_PACK, st, [&] { return nsk::launch_pack(pp, st); }) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
 
+// ------------------------------------------------------ fp32-Gram path
+// Workspace per bucket (fp32): X sets 0 and 1 = [X hi | X lo | X^T hi | X^T lo]
+// of cnt * m_pad * n_pad each; A = [hi | lo], B = [hi | lo] of cnt * m_pad^2.
+struct Bucket32Ptrs {
+  float* x[2];   // set base (X hi); X lo, X^T hi, X^T lo follow at xs apart
+  float* a;      // A hi; A lo at as apart
+  float* b;
+  long long xs, as;
+};
+
+Bucket32Ptrs bucket32_ptrs(const Bucket& b, char* ws) {
+  Bucket32Ptrs q;
+  const long long cnt = static_cast<long long>(b.members.size());
+  q.xs = cnt * b.m_pad * b.n_pad;
+  q.as = cnt * b.m_pad * b.m_pad;
+  q.x[0] = reinterpret_cast<float*>(ws + b.off_x0);
+  q.x[1] = reinterpret_cast<float*>(ws + b.off_x1);
+  q.a = reinterpret_cast<float*>(ws + b.off_a);
+  q.b = reinterpret_cast<float*>(ws + b.off_b);
+  return q;
+}
+
+// 3-D fp32 tensor map over [count][outer][inner], box {32, 128, 1}, 128-byte swizzle.
+int make_map32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count) {
+  cuuint64_t dims[3] = {inner, outer, count};
+  cuuint64_t strides[2] = {inner * 4, inner * outer * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
+}
+
+template <typename P>
+int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, size_t b1, unsigned int* status,
+                 void* const* final_out) {
+  std::memset(&gp, 0, sizeof(gp));
+  gp.alpha = p.a;
+  gp.beta = p.b;
+  gp.gamma = p.c;
+  gp.status = status;
+  long long tiles = 0;
+  int nb = 0, n_out = 0;
+  for (size_t bi = b0; bi < b1; ++bi, ++nb) {
+    const Bucket& b = p.buckets[bi];
+    const Bucket32Ptrs q = bucket32_ptrs(b, ws);
+    const uint64_t cnt = b.members.size();
+    nsk::Gemm32Bucket& g = gp.bk[nb];
+    g.tile_begin = tiles;
+    g.count = static_cast<int>(cnt);
+    g.m_valid = static_cast<int>(b.m);
+    g.n_valid = static_cast<int>(b.n);
+    g.cols_valid = static_cast<int>(b.m_pad);
+    int rc = NS_OK;
+    if (phase == nsk::PH32_GRAM || phase == nsk::PH32_A2B) {
+      g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
+      g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
+      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
+      g.ld = static_cast<int>(b.m_pad);
+      g.mat_stride = b.m_pad * b.m_pad;
+      if (phase == nsk::PH32_GRAM) {
+        float* xh = q.x[cur];
+        float* xl = xh + q.xs;
+        g.k_blocks = static_cast<int>(b.n_pad / 32);
+        g.out_h = q.a;
+        g.out_l = q.a + q.as;
+        rc = make_map32(&gp.tmah[nb], xh, b.n_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmal[nb], xl, b.n_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmbh[nb], xh, b.n_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmbl[nb], xl, b.n_pad, b.m_pad, cnt);
+      } else {
+        g.k_blocks = static_cast<int>(b.m_pad / 32);
+        g.out_h = q.b;
+        g.out_l = q.b + q.as;
+        g.aux_h = q.a;
+        g.aux_l = q.a + q.as;
+        rc = make_map32(&gp.tmah[nb], q.a, b.m_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmal[nb], q.a + q.as, b.m_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmbh[nb], q.a, b.m_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = make_map32(&gp.tmbl[nb], q.a + q.as, b.m_pad, b.m_pad, cnt);
+      }
+    } else {
+      // (B X)^T = X^T B: M over n (X^T rows), N over m (B rows), K = m
+      float* xc = q.x[cur];
+      float* xn = q.x[1 - cur];
+      g.tiles_m = static_cast<int>(b.n_pad / nsk::GEMM_BM);
+      g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
+      g.tiles_per_mat = g.tiles_m * g.tiles_n;
+      g.k_blocks = static_cast<int>(b.m_pad / 32);
+      g.ld = static_cast<int>(b.n_pad);
+      g.ld_t = static_cast<int>(b.m_pad);
+      g.mat_stride = b.m_pad * b.n_pad;
+      g.mat_stride_t = b.m_pad * b.n_pad;
+      g.aux_h = xc;
+      g.aux_l = xc + q.xs;
+      g.out_h = xn;
+      g.out_l = xn + q.xs;
+      g.out_th = xn + 2 * q.xs;
+      g.out_tl = xn + 3 * q.xs;
+      rc = make_map32(&gp.tmah[nb], xc + 2 * q.xs, b.m_pad, b.n_pad, cnt);
+      if (rc == NS_OK) rc = make_map32(&gp.tmal[nb], xc + 3 * q.xs, b.m_pad, b.n_pad, cnt);
+      if (rc == NS_OK) rc = make_map32(&gp.tmbh[nb], q.b, b.m_pad, b.m_pad, cnt);
+      if (rc == NS_OK) rc = make_map32(&gp.tmbl[nb], q.b + q.as, b.m_pad, b.m_pad, cnt);
+      if (final_out) {
+        g.out_first = n_out;
+        for (size_t s = 0; s < cnt; ++s) {
+          const Tensor& t = p.t[b.members[s]];
+          const unsigned long long a = reinterpret_cast<unsigned long long>(final_out[t.ordinal]);
+          gp.out_tab[n_out++] = a | (t.transposed ? 1ull : 0ull);
+        }
+      }
+    }
+    if (rc != NS_OK) return rc;
+    tiles += static_cast<long long>(g.tiles_per_mat) * static_cast<long long>(cnt);
+  }
+  gp.nb = nb;
+  gp.total_tiles = tiles;
+  return NS_OK;
+}
+
+int orthogonalize_f32(const Plan& p, const void* const* in, void* const* out, char* ws, int nsm,
+                      unsigned int* status, cudaStream_t st) {
+  // prologue: sums of squares, scales, X_0 hi/lo in both orientations
+  for (const Bucket& b : p.buckets) {
+    const BucketPtrs q0 = bucket_ptrs(b, ws);
+    const Bucket32Ptrs q = bucket32_ptrs(b, ws);
+    const size_t cnt = b.members.size();
+    for (size_t s0 = 0; s0 < cnt; s0 += nsk::PRO_MAX_MATS) {
+      nsk::ProParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.count = static_cast<int>(std::min<size_t>(nsk::PRO_MAX_MATS, cnt - s0));
+      pp.nchunks = static_cast<int>(b.nchunks);
+      pp.m_pad = static_cast<int>(b.m_pad);
+      pp.n_pad = static_cast<int>(b.n_pad);
+      pp.m = static_cast<int>(b.m);
+      pp.n = static_cast<int>(b.n);
+      pp.eps = p.eps;
+      pp.out_f32 = 1;
+      pp.x_split = q.xs;
+      pp.status = status;
+      for (int k = 0; k < pp.count; ++k) {
+        const size_t s = s0 + k;
+        const Tensor& t = p.t[b.members[s]];
+        nsk::MatDesc& d = pp.md[k];
+        d.in = in[t.ordinal];
+        d.out = out[t.ordinal];
+        d.x = q.x[0] + s * b.m_pad * b.n_pad;
+        d.partial = q0.partial + s * b.nchunks;
+        d.scale = q0.scale + s;
+        d.numel = t.numel;
+        d.rows = static_cast<int>(t.rows);
+        d.cols = static_cast<int>(t.cols);
+        d.transposed = t.transposed ? 1 : 0;
+      }
+      if (counted(K_PRO, st, [&] { return nsk::launch_sumsq(pp, st); }) != cudaSuccess ||
+          counted(K_PRO, st, [&] { return nsk::launch_scale(pp, st); }) != cudaSuccess ||
+          counted(K_PRO, st, [&] { return nsk::launch_prep32(pp, st); }) != cudaSuccess)
+        return NS_ERR_CUDA;
+    }
+  }
+  std::vector<char> stored(p.buckets.size(), 0);
+  int cur = 0;
+  for (int step = 0; step < p.steps; ++step) {
+    const bool last = step + 1 == p.steps;
+    for (int phase = nsk::PH32_GRAM; phase <= nsk::PH32_BXT; ++phase) {
+      for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
+        const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
+        int rc;
+        if (last && phase == nsk::PH32_BXT && group_matrices(p, b0, b1) <= size_t(nsk::GEMM32_MAX_OUT)) {
+          static thread_local nsk::Gemm32FinalParams gp;
+          rc = fill_phase32(gp, p, ws, phase, cur, b0, b1, status, out);
+          if (rc != NS_OK) return rc;
+          const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
+          if (counted(K_BX, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
+            return NS_ERR_CUDA;
+          for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
+        } else {
+          nsk::Gemm32Params gp;
+          rc = fill_phase32(gp, p, ws, phase, cur, b0, b1, status, nullptr);
+          if (rc != NS_OK) return rc;
+          const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
+          if (counted(phase, st, [&] { return nsk::launch_gemm32(phase, gp, grid, st); }) != cudaSuccess)
+            return NS_ERR_CUDA;
+        }
+        if (phase == nsk::PH32_GRAM && p.ridge > 0.0f) {
+          nsk::Ridge32Params rp;
+          std::memset(&rp, 0, sizeof(rp));
+          rp.ridge = p.ridge;
+          for (size_t bi = b0; bi < b1; ++bi) {
+            const Bucket& b = p.buckets[bi];
+            const Bucket32Ptrs q = bucket32_ptrs(b, ws);
+            nsk::Ridge32Bucket& r = rp.bk[rp.nb++];
+            r.ah = q.a;
+            r.al = q.a + q.as;
+            r.mat_stride = b.m_pad * b.m_pad;
+            r.ld = static_cast<int>(b.m_pad);
+            r.m = static_cast<int>(b.m);
+            r.count = static_cast<int>(b.members.size());
+            rp.max_count = std::max(rp.max_count, r.count);
+          }
+          if (counted(K_PRO, st, [&] { return nsk::launch_ridge32(rp, st); }) != cudaSuccess) return NS_ERR_CUDA;
+        }
+      }
+    }
+    cur = 1 - cur;
+  }
+  for (size_t bi = 0; bi < p.buckets.size(); ++bi) {
+    if (stored[bi]) continue;
+    const Bucket& b = p.buckets[bi];
+    const Bucket32Ptrs q = bucket32_ptrs(b, ws);
+    const size_t cnt = b.members.size();
+    for (size_t s0 = 0; s0 < cnt; s0 += nsk::PRO_MAX_MATS) {
+      nsk::ProParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.count = static_cast<int>(std::min<size_t>(nsk::PRO_MAX_MATS, cnt - s0));
+      pp.m_pad = static_cast<int>(b.m_pad);
+      pp.n_pad = static_cast<int>(b.n_pad);
+      pp.m = static_cast<int>(b.m);
+      pp.n = static_cast<int>(b.n);
+      pp.out_f32 = 1;
+      pp.x_split = q.xs;
+      pp.status = status;
+      for (int k = 0; k < pp.count; ++k) {
+        const size_t s = s0 + k;
+        const Tensor& t = p.t[b.members[s]];
+        nsk::MatDesc& d = pp.md[k];
+        d.out = out[t.ordinal];
+        d.xfinal = q.x[cur] + s * b.m_pad * b.n_pad;
+        d.rows = static_cast<int>(t.rows);
+        d.cols = static_cast<int>(t.cols);
+        d.transposed = t.transposed ? 1 : 0;
+        d.numel = t.numel;
+      }
+      if (counted(K_PRO, st, [&] { return nsk::launch_store32(pp, st); }) != cudaSuccess) return NS_ERR_CUDA;
+    }
+  }
+  return NS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -343,7 +583,6 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
     const Tensor& t = p.t[p.part[j]];
     if (t.numel > 0 && (!in[j] || !out[j])) return NS_ERR_ARG;
   }
-  if (p.gram_mode != NS_BF16) return NS_ERR_UNSUPPORTED;
   if (p.buckets.empty()) return NS_OK;
   if (!workspace || workspace_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return NS_ERR_WORKSPACE;
@@ -354,6 +593,7 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
   if (rc != NS_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  if (p.gram_mode == NS_FP32_GRAM) return orthogonalize_f32(p, in, out, ws, nsm, status, st);
 
   // prologue: sums of squares, scales, X_0 = scale * (T or T^T), zero padded
   for (const Bucket& b : p.buckets) {

@@ -1,0 +1,392 @@
+// fp32-Gram variant of the three Newton-Schulz products (Megatron-Core API page
+// owner_planning, ns_cost_fn; Megatron-LM issue #6720 pairs an fp32/TF32 Gram
+// with a trace ridge to harden the iteration):
+//
+//   PH32_GRAM  A  = X X^T                 symmetric: upper tiles + mirror
+//   PH32_A2B   B  = b A + c (A A)         symmetric: upper tiles + mirror
+//   PH32_BXT   X' = a X + B X, computed as (B X)^T = X^T B (B symmetric)
+//
+// Every matrix is held in fp32 as a pair (hi, lo): hi = x rounded to TF32,
+// lo = x - hi. Each product is accumulated in fp32 TMEM from three TF32
+// tensor-core products hi*hi + hi*lo + lo*hi (the split-precision scheme of
+// Markidis et al. 2018 and Ootomo & Yokota 2022), which keeps fp32-level
+// accuracy; the dropped lo*lo term is ~2^-22 relative.
+//
+// All operands are K-major (rows of 32 fp32 = 128 bytes, 128-byte swizzle):
+// X is kept both as X (m_pad x n_pad, for the Gram) and X^T (n_pad x m_pad,
+// for B*X), and the B*X epilogue writes both copies of the next X.
+// Structure as in gemm.cu: persistent CTAs, a TMA producer thread, one MMA
+// issuing thread (tcgen05.mma.cta_group::1.kind::tf32, M=128, N=256, K=8),
+// two TMEM accumulators, four epilogue warps; every wait is bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nsk {
+namespace {
+
+using namespace nsptx;
+
+constexpr int BM = 128, BN = 256, BK = 32, UK = 8;
+constexpr int STAGES = 2;
+constexpr uint32_t A_BYTES = BM * BK * 4;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 4;  // 32 KB
+constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // hi and lo of both operands
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+template <int PHASE, typename P>
+__device__ __forceinline__ void decode_tile32(const P& p, long long t, int& b, int& mat, int& tm, int& tn) {
+  b = 0;
+  while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
+  const Gemm32Bucket& B = p.bk[b];
+  const long long local = t - B.tile_begin;
+  mat = static_cast<int>(local / B.tiles_per_mat);
+  int r = static_cast<int>(local % B.tiles_per_mat);
+  if (PHASE == PH32_BXT) {
+    tm = r / B.tiles_n;
+    tn = r % B.tiles_n;
+  } else {
+    tm = 0;
+    while (true) {
+      const int tn0 = (tm * BM) / BN;
+      const int cnt = B.tiles_n - tn0;
+      if (r < cnt) {
+        tn = tn0 + r;
+        break;
+      }
+      r -= cnt;
+      ++tm;
+    }
+  }
+}
+
+template <int PHASE, bool FINAL, typename P>
+__global__ void __launch_bounds__(THREADS, 1) ns_gemm32_kernel(const __grid_constant__ P p) {
+  static_assert(!FINAL || PHASE == PH32_BXT, "only the B*X phase has a final-store form");
+  constexpr bool SYRK = (PHASE != PH32_BXT);
+  constexpr uint32_t IDESC = idesc_make(2u, BM, BN, false, false);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // stage s: [A hi | A lo | B hi | B lo]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (blockDim.x != THREADS) {
+    if (threadIdx.x == 0) atomicOr(p.status, NS_DEV_BAD_LAUNCH);
+    return;
+  }
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    for (int b = 0; b < p.nb; ++b) {
+      prefetch_tmap(&p.tmah[b]);
+      prefetch_tmap(&p.tmal[b]);
+      prefetch_tmap(&p.tmbh[b]);
+      prefetch_tmap(&p.tmbl[b]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    long long issued = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile32<PHASE>(p, t, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
+        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        uint8_t* base = smem + stage * STAGE_BYTES;
+        tma_load_3d(base, &p.tmah[b], &full[stage], kb * BK, tm * BM, mat);
+        tma_load_3d(base + A_BYTES, &p.tmal[b], &full[stage], kb * BK, tm * BM, mat);
+        uint8_t* bh = base + 2 * A_BYTES;
+        uint8_t* bl = bh + B_BYTES;
+        tma_load_3d(bh, &p.tmbh[b], &full[stage], kb * BK, tn * BN, mat);
+        tma_load_3d(bh + 128 * 128, &p.tmbh[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        tma_load_3d(bl, &p.tmbl[b], &full[stage], kb * BK, tn * BN, mat);
+        tma_load_3d(bl + 128 * 128, &p.tmbl[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    if (*abort_flag) {
+      const long long first = issued > STAGES ? issued - STAGES : 0;
+      for (long long i = first; i < issued; ++i)
+        mbar_wait_drain(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.status);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ----------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile32<PHASE>(p, t, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto mma_done;
+        tc_fence_after();
+        const uint32_t ah = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t al = ah + A_BYTES;
+        const uint32_t bh = ah + 2 * A_BYTES;
+        const uint32_t bl = bh + B_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k) {
+          const uint32_t o = k * (UK * 4);  // 32 bytes per K step inside the 128-byte row
+          const uint32_t first = (kb | k) != 0 ? 1u : 0u;
+          mma_tf32(d_tmem, sdesc_sw128(ah + o, 16, 1024), sdesc_sw128(bh + o, 16, 1024), IDESC, first);
+          mma_tf32(d_tmem, sdesc_sw128(ah + o, 16, 1024), sdesc_sw128(bl + o, 16, 1024), IDESC, 1u);
+          mma_tf32(d_tmem, sdesc_sw128(al + o, 16, 1024), sdesc_sw128(bh + o, 16, 1024), IDESC, 1u);
+        }
+        mma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit(&tfull[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  mma_done:
+    if (*abort_flag) {
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.status);
+    }
+  } else if (warp >= 2) {
+    // -------------------------------------------------------------- epilogue
+    const int lg = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mat, tm, tn;
+      decode_tile32<PHASE>(p, t, b, mat, tm, tn);
+      const Gemm32Bucket& B = p.bk[b];
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int r0w = tm * BM + lg * 32;
+      const int r = r0w + lane;  // Gram/A2B: row of A/B; BXT: column j of X (n index)
+      const long long mo = static_cast<long long>(mat) * B.mat_stride;
+      const long long mt = static_cast<long long>(mat) * B.mat_stride_t;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int cg = tn * BN + c0;
+        if (cg >= B.cols_valid) break;
+        if (SYRK && cg + 31 < r0w) continue;
+        uint32_t v[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + acc * BN + c0, v);
+        tmem_ld_wait();
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (PHASE == PH32_A2B) {
+          // B = b*A + c*(A A); A = hi + lo
+          const float4* h4 = reinterpret_cast<const float4*>(B.aux_h + mo + static_cast<long long>(r) * B.ld + cg);
+          const float4* l4 = reinterpret_cast<const float4*>(B.aux_l + mo + static_cast<long long>(r) * B.ld + cg);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 h = h4[q], l = l4[q];
+            f[4 * q + 0] = p.beta * (h.x + l.x) + p.gamma * f[4 * q + 0];
+            f[4 * q + 1] = p.beta * (h.y + l.y) + p.gamma * f[4 * q + 1];
+            f[4 * q + 2] = p.beta * (h.z + l.z) + p.gamma * f[4 * q + 2];
+            f[4 * q + 3] = p.beta * (h.w + l.w) + p.gamma * f[4 * q + 3];
+          }
+        }
+        if (SYRK) {
+          float fh[32], fl[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            fh[j] = tf32_round(f[j]);
+            fl[j] = f[j] - fh[j];
+          }
+          float* oh = B.out_h + mo + static_cast<long long>(r) * B.ld + cg;
+          float* ol = B.out_l + mo + static_cast<long long>(r) * B.ld + cg;
+          if (cg >= r) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              reinterpret_cast<float4*>(oh)[q] = make_float4(fh[4 * q], fh[4 * q + 1], fh[4 * q + 2], fh[4 * q + 3]);
+              reinterpret_cast<float4*>(ol)[q] = make_float4(fl[4 * q], fl[4 * q + 1], fl[4 * q + 2], fl[4 * q + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (cg + j >= r) {
+                oh[j] = fh[j];
+                ol[j] = fl[j];
+              }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = cg + j;
+            if (c > r) {
+              B.out_h[mo + static_cast<long long>(c) * B.ld + r] = fh[j];
+              B.out_l[mo + static_cast<long long>(c) * B.ld + r] = fl[j];
+            }
+          }
+        } else {
+          // acc[r][c] = (B X)[c][r]: c = m index (cg + j), r = n index.
+          // X'[c][r] = a * X[c][r] + acc; X = hi + lo, read column-wise (lanes
+          // hold consecutive r, so each access is contiguous across the warp).
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const long long e = mo + static_cast<long long>(cg + j) * B.ld + r;
+            f[j] = p.alpha * (B.aux_h[e] + B.aux_l[e]) + f[j];
+          }
+          if (FINAL) {
+            if (r < B.n_valid) {
+              const unsigned long long ent = p.out_tab[B.out_first + mat];
+              float* o = reinterpret_cast<float*>(ent & ~1ull);
+              if (!(ent & 1ull)) {
+                // output rows x cols = m x n: element (c, r)
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.m_valid) o[static_cast<long long>(cg + j) * B.n_valid + r] = f[j];
+              } else {
+                // transposed tensor: output n x m, element (r, c), contiguous per thread
+                float* dst = o + static_cast<long long>(r) * B.m_valid + cg;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.m_valid) dst[j] = f[j];
+              }
+            }
+            continue;
+          }
+          float fh[32], fl[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            fh[j] = tf32_round(f[j]);
+            fl[j] = f[j] - fh[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const long long e = mo + static_cast<long long>(cg + j) * B.ld + r;
+            B.out_h[e] = fh[j];
+            B.out_l[e] = fl[j];
+          }
+          float* th = B.out_th + mt + static_cast<long long>(r) * B.ld_t + cg;
+          float* tl = B.out_tl + mt + static_cast<long long>(r) * B.ld_t + cg;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            reinterpret_cast<float4*>(th)[q] = make_float4(fh[4 * q], fh[4 * q + 1], fh[4 * q + 2], fh[4 * q + 3]);
+            reinterpret_cast<float4*>(tl)[q] = make_float4(fl[4 * q], fl[4 * q + 1], fl[4 * q + 2], fl[4 * q + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int PHASE, bool FINAL, typename P>
+cudaError_t launch32(const P& p, int grid, cudaStream_t st) {
+  auto kern = ns_gemm32_kernel<PHASE, FINAL, P>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  return cudaGetLastError();
+}
+
+// Trace ridge: A <- A + ridge * (trace(A) / m) * I on the (hi, lo) pair.
+// One CTA per matrix; fixed-order reduction.
+__global__ void __launch_bounds__(256) ns_ridge32_kernel(const __grid_constant__ Ridge32Params p) {
+  const Ridge32Bucket& B = p.bk[blockIdx.y];
+  if (static_cast<int>(blockIdx.x) >= B.count) return;
+  float* ah = B.ah + static_cast<long long>(blockIdx.x) * B.mat_stride;
+  float* al = B.al + static_cast<long long>(blockIdx.x) * B.mat_stride;
+  __shared__ double red[256];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < B.m; i += blockDim.x) {
+    const long long d = static_cast<long long>(i) * B.ld + i;
+    s += static_cast<double>(ah[d]) + static_cast<double>(al[d]);
+  }
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  const float delta = static_cast<float>(static_cast<double>(p.ridge) * red[0] / B.m);
+  __syncthreads();
+  for (int i = threadIdx.x; i < B.m; i += blockDim.x) {
+    const long long d = static_cast<long long>(i) * B.ld + i;
+    const float v = ah[d] + al[d] + delta;
+    const float h = tf32_round(v);
+    ah[d] = h;
+    al[d] = v - h;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm32(int phase, const Gemm32Params& p, int grid, cudaStream_t st) {
+  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+  switch (phase) {
+    case PH32_GRAM: return launch32<PH32_GRAM, false>(p, grid, st);
+    case PH32_A2B: return launch32<PH32_A2B, false>(p, grid, st);
+    case PH32_BXT: return launch32<PH32_BXT, false>(p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int grid, cudaStream_t st) {
+  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+  return launch32<PH32_BXT, true>(p, grid, st);
+}
+
+cudaError_t launch_ridge32(const Ridge32Params& p, cudaStream_t st) {
+  if (p.nb <= 0 || p.max_count <= 0) return cudaSuccess;
+  ns_ridge32_kernel<<<dim3(p.max_count, p.nb), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nsk

@@ -52,14 +52,68 @@ static_assert(sizeof(GemmFinalParams) <= 32764, "kernel parameter block too larg
 
 constexpr int GEMM_BM = 128, GEMM_BN = 256, GEMM_BK = 64;
 
+// ----------------------------------------------------- fp32-Gram GEMMs
+enum Gemm32Phase { PH32_GRAM = 0, PH32_A2B = 1, PH32_BXT = 2 };
+
+struct Gemm32Bucket {
+  long long tile_begin;
+  long long mat_stride;    // elements between matrices of the m-major buffers (A, B or X)
+  long long mat_stride_t;  // elements between matrices of the transposed X buffers
+  float* out_h;            // Gram: A hi; A2B: B hi; BXT: next X hi (m_pad x n_pad)
+  float* out_l;
+  float* out_th;           // BXT: next X^T hi (n_pad x m_pad)
+  float* out_tl;
+  const float* aux_h;      // A2B: A hi; BXT: current X hi
+  const float* aux_l;
+  int count, tiles_m, tiles_n, tiles_per_mat, k_blocks;
+  int ld;                  // leading dimension of out_h/out_l/aux (elements)
+  int ld_t;                // leading dimension of out_th/out_tl
+  int cols_valid;          // tile columns that exist (m_pad)
+  int m_valid, n_valid;    // unpadded m, n (final-store launches)
+  int out_first;
+};
+
+constexpr int GEMM32_MAX_OUT = 3200;
+
+template <int NOUT>
+struct Gemm32ParamsT {
+  CUtensorMap tmah[GEMM_MAX_BUCKETS];  // A operand hi / lo, K-major, box {32, 128, 1} fp32
+  CUtensorMap tmal[GEMM_MAX_BUCKETS];
+  CUtensorMap tmbh[GEMM_MAX_BUCKETS];  // B operand hi / lo, K-major, box {32, 128, 1} fp32
+  CUtensorMap tmbl[GEMM_MAX_BUCKETS];
+  Gemm32Bucket bk[GEMM_MAX_BUCKETS];
+  long long total_tiles;
+  int nb;
+  float alpha, beta, gamma;
+  unsigned int* status;
+  unsigned long long out_tab[NOUT];
+};
+using Gemm32Params = Gemm32ParamsT<1>;
+using Gemm32FinalParams = Gemm32ParamsT<GEMM32_MAX_OUT>;
+static_assert(sizeof(Gemm32FinalParams) <= 32764, "kernel parameter block too large");
+
+struct Ridge32Bucket {
+  float* ah;
+  float* al;
+  long long mat_stride;
+  int ld, m, count;
+};
+
+struct Ridge32Params {
+  Ridge32Bucket bk[GEMM_MAX_BUCKETS];
+  int nb, max_count;
+  float ridge;
+};
+
 // ------------------------------------------------------- prologue / store
 constexpr int PRO_MAX_MATS = 192;
 
 struct MatDesc {
   const void* in;       // original tensor, row-major (rows x cols), bf16
   void* out;            // result, row-major (rows x cols)
-  void* x;              // this matrix's X_0 in the workspace (m_pad x n_pad, bf16)
-  const void* xfinal;   // this matrix's X_k in the workspace
+  void* x;              // this matrix's X_0 in the workspace (m_pad x n_pad, bf16;
+                        // fp32-Gram: X hi, with X lo, X^T hi, X^T lo at x_split apart)
+  const void* xfinal;   // this matrix's X_k in the workspace (fp32-Gram: X hi; X lo at x_split)
   float* partial;       // nchunks partial sums of squares
   float* scale;         // 1 / (||X||_F + eps)
   long long numel;
@@ -75,6 +129,7 @@ struct ProParams {
   int m, n;             // valid dims after the transpose
   float eps;
   int out_f32;          // result dtype: 0 bf16, 1 fp32
+  long long x_split;    // fp32-Gram: elements between the X hi / X lo / X^T hi / X^T lo buffers
   unsigned int* status;
 };
 
@@ -113,5 +168,10 @@ cudaError_t launch_scale(const ProParams& p, cudaStream_t st);
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st);
 cudaError_t launch_store(const ProParams& p, cudaStream_t st);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t st);
+cudaError_t launch_gemm32(int phase, const Gemm32Params& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int grid, cudaStream_t st);
+cudaError_t launch_ridge32(const Ridge32Params& p, cudaStream_t st);
+cudaError_t launch_prep32(const ProParams& p, cudaStream_t st);
+cudaError_t launch_store32(const ProParams& p, cudaStream_t st);
 
 }  // namespace nsk

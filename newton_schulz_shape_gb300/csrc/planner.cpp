@@ -94,7 +94,8 @@ int finish(Plan& p) {
       b.m = t.m;
       b.n = t.n;
       b.m_pad = round_up(t.m, nsk::GEMM_BM);
-      b.n_pad = round_up(t.n, nsk::GEMM_BK);
+      // fp32-Gram: n is also the M dimension of the (B X)^T product, tiled by 128
+      b.n_pad = round_up(t.n, p.gram_mode == NS_FP32_GRAM ? nsk::GEMM_BM : nsk::GEMM_BK);
       index[key] = static_cast<int>(p.buckets.size());
       p.buckets.push_back(b);
       it = index.find(key);
@@ -107,7 +108,12 @@ int finish(Plan& p) {
     const double wy = double(y.m) * double(y.m) * double(y.n);
     return wx > wy;
   });
-  const uint64_t xb = p.gram_mode == NS_FP32_GRAM ? 4 : 2;
+  // bf16 path: one bf16 copy of X per ping-pong buffer, A and B in bf16.
+  // fp32-Gram path: X as (hi, lo) fp32 pairs, both m-major and transposed
+  // (4 buffers per ping-pong set); A and B as (hi, lo) fp32 pairs.
+  const bool f32 = p.gram_mode == NS_FP32_GRAM;
+  const uint64_t xset = f32 ? 4 * 4 : 2;
+  const uint64_t aset = f32 ? 2 * 4 : 2;
   uint64_t off = 0;
   auto take = [&](uint64_t bytes) {
     off = (off + 1023) / 1024 * 1024;
@@ -122,8 +128,8 @@ int finish(Plan& p) {
       p.t[b.members[s]].bucket = static_cast<int>(bi);
       p.t[b.members[s]].slot = static_cast<int>(s);
     }
-    const uint64_t xbytes = cnt * uint64_t(b.m_pad) * uint64_t(b.n_pad) * xb;
-    const uint64_t abytes = cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * xb;
+    const uint64_t xbytes = cnt * uint64_t(b.m_pad) * uint64_t(b.n_pad) * xset;
+    const uint64_t abytes = cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * aset;
     b.off_x0 = take(xbytes);
     b.off_x1 = take(xbytes);
     b.off_a = take(abytes);

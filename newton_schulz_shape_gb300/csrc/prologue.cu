@@ -212,7 +212,108 @@ __global__ void __launch_bounds__(256) ns_store_kernel(const __grid_constant__ P
   }
 }
 
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// fp32-Gram prologue: one 64 x 64 tile of X_0 = scale * V per CTA, written as
+// hi/lo TF32 pairs both as X (m_pad x n_pad) and as X^T (n_pad x m_pad).
+__global__ void __launch_bounds__(256) ns_prep32_kernel(const __grid_constant__ ProParams p) {
+  __shared__ float tile[TILE][TILE + 1];
+  const MatDesc& d = p.md[blockIdx.y];
+  const float s = *d.scale;
+  const unsigned short* src = reinterpret_cast<const unsigned short*>(d.in);
+  float* xh = reinterpret_cast<float*>(d.x);
+  float* xl = xh + p.x_split;
+  float* th = xh + 2 * p.x_split;
+  float* tl = xh + 3 * p.x_split;
+  const int tiles_n = p.n_pad / TILE;
+  const int ti = blockIdx.x / tiles_n, tj = blockIdx.x % tiles_n;
+  const int i0 = ti * TILE, j0 = tj * TILE;
+  const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;
+  if (!d.transposed) {
+    for (int ii = ty; ii < TILE; ii += 4) {   // V[i][j] = T[i][j], coalesced along j
+      const int i = i0 + ii, j = j0 + tx;
+      tile[ii][tx] = (i < p.m && j < p.n) ? s * bf16_to_f(src[static_cast<long long>(i) * p.n + j]) : 0.0f;
+    }
+  } else {
+    for (int jj = ty; jj < TILE; jj += 4) {   // V[i][j] = T[j][i], coalesced along i
+      const int j = j0 + jj, i = i0 + tx;
+      tile[tx][jj] = (i < p.m && j < p.n) ? s * bf16_to_f(src[static_cast<long long>(j) * p.m + i]) : 0.0f;
+    }
+  }
+  __syncthreads();
+  for (int ii = ty; ii < TILE; ii += 4) {     // X rows
+    const float v = tile[ii][tx], h = tf32_round(v);
+    const long long e = static_cast<long long>(i0 + ii) * p.n_pad + j0 + tx;
+    xh[e] = h;
+    xl[e] = v - h;
+  }
+  for (int jj = ty; jj < TILE; jj += 4) {     // X^T rows
+    const float v = tile[tx][jj], h = tf32_round(v);
+    const long long e = static_cast<long long>(j0 + jj) * p.m_pad + i0 + tx;
+    th[e] = h;
+    tl[e] = v - h;
+  }
+}
+
+// fp32-Gram store (used when the last B*X launch could not store directly):
+// out (rows x cols, fp32) from X_k = hi + lo.
+__global__ void __launch_bounds__(256) ns_store32_kernel(const __grid_constant__ ProParams p) {
+  __shared__ float tile[TILE][TILE + 1];
+  const MatDesc& d = p.md[blockIdx.y];
+  const int rows = d.rows, cols = d.cols;
+  const int tiles_c = (cols + TILE - 1) / TILE;
+  const int ti = blockIdx.x / tiles_c, tj = blockIdx.x % tiles_c;
+  const int i0 = ti * TILE, j0 = tj * TILE;
+  const float* xh = reinterpret_cast<const float*>(d.xfinal);
+  const float* xl = xh + p.x_split;
+  float* out = reinterpret_cast<float*>(d.out);
+  const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;
+  if (!d.transposed) {
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      if (i < rows && j < cols) {
+        const long long e = static_cast<long long>(i) * p.n_pad + j;
+        out[static_cast<long long>(i) * cols + j] = xh[e] + xl[e];
+      }
+    }
+  } else {
+    for (int jj = ty; jj < TILE; jj += 4) {
+      const int j = j0 + jj, i = i0 + tx;
+      float v = 0.0f;
+      if (i < rows && j < cols) {
+        const long long e = static_cast<long long>(j) * p.n_pad + i;
+        v = xh[e] + xl[e];
+      }
+      tile[jj][tx] = v;
+    }
+    __syncthreads();
+    for (int ii = ty; ii < TILE; ii += 4) {
+      const int i = i0 + ii, j = j0 + tx;
+      if (i < rows && j < cols) out[static_cast<long long>(i) * cols + j] = tile[tx][ii];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prep32(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0) return cudaSuccess;
+  const int tiles = (p.m_pad / TILE) * (p.n_pad / TILE);
+  ns_prep32_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_store32(const ProParams& p, cudaStream_t st) {
+  if (p.count <= 0) return cudaSuccess;
+  const int rows = p.md[0].rows, cols = p.md[0].cols;
+  const int tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
+  ns_store32_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0 || p.nchunks <= 0) return cudaSuccess;

@@ -1,0 +1,96 @@
+"""GPU parity of the fp32-Gram path (NS_FP32_GRAM) against the float64 oracle.
+
+Bar (per matrix): relative Frobenius error <= 1e-3. Inputs are bf16 (the
+momentum shards the pack moves); results are fp32. The trace ridge is
+compared with the oracle's reading of it, A <- A + ridge * (tr A / m) * I
+before B is formed (parity unpinned: the pages do not fix the form).
+"""
+
+import pytest
+import torch
+
+import workloads
+from gpu_util import oracle_ns, rel_err
+from oracle import ns as ons
+
+pytestmark = pytest.mark.gpu
+nsg = pytest.importorskip("newton_schulz_shape_gb300")
+
+FP32_TOL = 1e-3
+
+
+def run_f32(shapes, ts, steps=workloads.STEPS, ridge=0.0, fixed_ws=False):
+    dev = torch.device("cuda:0")
+    ins = [t.to(dev) for t in ts]
+    outs = [torch.full(t.shape, float("nan"), dtype=torch.float32, device=dev) for t in ins]
+    plan = nsg.ns_plan_create(shapes, steps=steps, eps=workloads.EPS, gram_mode=nsg.NS_FP32_GRAM, ridge=ridge, S=1)
+    assert plan.out_bytes == 4
+    if fixed_ws:
+        nsg.ns_orthogonalize_batched_fixed_ws(plan, ins, outs)
+    else:
+        ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    rc = nsg.ns_check_status(plan)
+    assert rc == nsg.NS_OK, nsg.ns_status_string(rc)
+    return outs
+
+
+def oracle(t, steps=workloads.STEPS, ridge=0.0):
+    return ons.newton_schulz(t.float().numpy(), steps, workloads.A_COEF, workloads.B_COEF, workloads.C_COEF,
+                             workloads.EPS, ridge=ridge)
+
+
+SHAPES = [(128, 256), (128, 256), (300, 700), (700, 300), (256, 64, 3, 3), (130, 130), (5, 3), (200, 456)]
+
+
+def test_fp32_gram_small_and_ragged():
+    ts = workloads.gen_tensors(workloads.Workload("f32", SHAPES, 1.0, 71))
+    outs = run_f32(SHAPES, ts)
+    for s, t, o in zip(SHAPES, ts, outs):
+        assert o.dtype == torch.float32 and o.shape == t.shape
+        err = rel_err(o, oracle(t))
+        assert err <= FP32_TOL, (s, err)
+
+
+@pytest.mark.parametrize("steps", [0, 1, 3])
+def test_fp32_gram_step_counts(steps):
+    shapes = [(192, 320), (320, 192)]
+    ts = workloads.gen_tensors(workloads.Workload("f32s", shapes, 0.02, 72))
+    outs = run_f32(shapes, ts, steps=steps)
+    for t, o in zip(ts, outs):
+        assert rel_err(o, oracle(t, steps)) <= FP32_TOL
+
+
+@pytest.mark.parametrize("ridge", [1e-5, 1e-3])
+def test_fp32_gram_trace_ridge(ridge):
+    shapes = [(256, 512), (512, 256), (100, 300)]
+    ts = workloads.gen_tensors(workloads.Workload("ridge", shapes, 0.02, 73))
+    outs = run_f32(shapes, ts, ridge=ridge)
+    for t, o in zip(ts, outs):
+        assert rel_err(o, oracle(t, ridge=ridge)) <= FP32_TOL
+        # the ridge moves the result measurably at 1e-3
+        if ridge >= 1e-3:
+            assert rel_err(o, oracle(t)) > 5 * rel_err(o, oracle(t, ridge=ridge))
+
+
+def test_fp32_gram_sweep_sizes():
+    shapes = [(1024, 2048), (2048, 1024), (1024, 1024)]
+    ts = workloads.gen_tensors(workloads.Workload("f32big", shapes, 0.02, 74))
+    outs = run_f32(shapes, ts)
+    for s, t, o in zip(shapes, ts, outs):
+        assert rel_err(o, oracle(t)) <= FP32_TOL, s
+
+
+def test_fp32_gram_beats_bf16_path():
+    shapes = [(256, 768)]
+    ts = workloads.gen_tensors(workloads.Workload("cmp", shapes, 0.02, 75))
+    ref = oracle(ts[0])
+    f32 = rel_err(run_f32(shapes, ts)[0], ref)
+    dev = torch.device("cuda:0")
+    x = ts[0].to(dev)
+    y = torch.empty_like(x)
+    plan = nsg.ns_plan_create(shapes, S=1)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    nsg.ns_orthogonalize_batched(plan, [x], [y], ws)
+    bf16 = rel_err(y, ref)
+    assert f32 < bf16 / 10, (f32, bf16)
