@@ -109,6 +109,28 @@ def traffic_for(kernel: str):
     return None
 
 
+# ------------------------------------------------------------- multi-rank
+def replica_seed(seed: int, rank: int, world: int) -> int:
+    """Each rank runs its own replica of the workload (weak scaling)."""
+    return seed + 7919 * rank if world > 1 else seed
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank time over all ranks (the only collective the bench uses)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(n_mats: int, world: int, ms_step: float) -> float:
+    """Whole-job matrices/s: every rank processes n_mats per step."""
+    return n_mats * world * 1000.0 / ms_step
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -239,8 +261,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     w = get_workload(args.workload, args.layers)
-    if world > 1:
-        w.seed += 7919 * rank      # each rank: its own replica of the workload
+    w.seed = replica_seed(w.seed, rank, world)
     S, shapes = w.S, w.shapes
     plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=S, shard_dim=0)
     home_off, home_sizes, rank_sizes = plan.home_layout()
@@ -316,17 +337,13 @@ def run_ours(args):
     rc = nsg.ns_check_status(plan, stream)
     if rc != nsg.NS_OK:
         raise RuntimeError(f"device status after timing: {nsg.ns_status_string(rc)}")
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
     pack_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     ns_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     unpack_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
     n_mats = len(shapes)
-    value = n_mats * world * 1000.0 / ms_step
+    value = job_value(n_mats, world, ms_step)
 
     # ---- raw copy bandwidth (context for e2e)
     copy_gbs = {}
@@ -391,15 +408,11 @@ def run_ours(args):
         stream.wait_stream(s_in)
         e1.record(stream)
         barrier()
-        ms_e2e = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
         # the results of the last step really came back
         ok = all(torch.equal(hout[(args.steps - 1) % 2][r], rank_out[r].cpu()) for r in range(S))
         nbytes = 2 * S * L
-        e2e = {"value": n_mats * world * 1000.0 / ms_e2e, "unit": UNIT, "ms_per_step": ms_e2e,
+        e2e = {"value": job_value(n_mats, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "pipelining": "copies of step k+1 (in) and k-1 (out) overlap step k's compute",
                "results_returned": ok, "copy_gbs": copy_gbs}
