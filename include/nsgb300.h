@@ -218,6 +218,13 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * is enabled, every launch is bracketed by two CUDA events recorded on the
  * stream it is launched on; ns_profile_read synchronises those events. */
 
+/* Tuning: how the bf16 GEMM phases tile the tensor cores. cl = 0 (default)
+ * pairs CTAs into 2-CTA clusters that share each B tile by TMA multicast
+ * whenever every bucket of a launch has at least two 128-row tile rows;
+ * cl = 1 never pairs; cl = 2 behaves like 0. Process-wide; results are the
+ * same up to fp32 summation order. */
+int ns_set_gemm_cluster(int cl);
+
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */
 int ns_profile_enable(int enable);
 

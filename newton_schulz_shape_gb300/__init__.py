@@ -231,3 +231,8 @@ def ns_profile_read(reset: bool = False):
     ms = (ctypes.c_double * 5)()
     check(lib.ns_profile_read(1 if reset else 0, n, ms), "ns_profile_read")
     return dict(zip(KERNEL_KINDS, list(n))), dict(zip(KERNEL_KINDS, list(ms)))
+
+
+def ns_set_gemm_cluster(cl: int) -> None:
+    """0: pair CTAs into B-sharing clusters when possible (default); 1: never."""
+    check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")

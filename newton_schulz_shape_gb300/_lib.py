@@ -62,6 +62,7 @@ _SIGS = {
     "ns_check_status": (ctypes.c_int, [_planp, ctypes.c_void_p]),
     "ns_orthogonalize_batched_fixed_ws": (ctypes.c_int, [_planp, _vpp, _vpp, ctypes.c_int, ctypes.c_void_p]),
     "ns_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+    "ns_set_gemm_cluster": (ctypes.c_int, [ctypes.c_int]),
     "ns_profile_read": (ctypes.c_int, [ctypes.c_int, _i64p, ctypes.POINTER(ctypes.c_double)]),
 }
 

@@ -40,6 +40,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+int g_force_cl = 0;  // 0: automatic; 1: never pair CTAs; 2: pair whenever possible
 
 // ----------------------------------------------------------- measurement
 constexpr int kKinds = 5;
@@ -143,10 +144,27 @@ int make_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_
   return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
 }
 
-long long syrk_tiles(int tiles_m, int tiles_n) {
+// Upper-triangle work items of one matrix: single tiles (cl = 1) or pairs of
+// tile rows 2q, 2q + 1 sharing their column tiles (cl = 2).
+long long syrk_tiles(int tiles_m, int tiles_n, int cl = 1) {
   long long t = 0;
-  for (int tm = 0; tm < tiles_m; ++tm) t += tiles_n - (tm * nsk::GEMM_BM) / nsk::GEMM_BN;
+  if (cl == 1) {
+    for (int tm = 0; tm < tiles_m; ++tm) t += tiles_n - (tm * nsk::GEMM_BM) / nsk::GEMM_BN;
+  } else {
+    for (int q = 0; q < (tiles_m + 1) / 2; ++q) t += tiles_n - q;
+  }
   return t;
+}
+
+// Cluster size for a launch: pairs of CTAs share B tiles when every bucket of
+// the launch has at least two tile rows.
+int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
+  for (size_t bi = b0; bi < b1; ++bi) {
+    const Bucket& b = p.buckets[bi];
+    if (b.m_pad / nsk::GEMM_BM < 2) return 1;
+  }
+  (void)phase;
+  return g_force_cl ? g_force_cl : 2;
 }
 
 struct BucketPtrs {
@@ -175,7 +193,7 @@ BucketPtrs bucket_ptrs(const Bucket& b, char* ws) {
 // entry is the output address with bit 0 set for transposed tensors.
 template <typename P>
 int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1,
-               unsigned int* status, void* const* final_out) {
+               unsigned int* status, void* const* final_out, int cl) {
   std::memset(&gp, 0, sizeof(gp));
   gp.alpha = p.a;
   gp.beta = p.b;
@@ -198,7 +216,7 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
     int rc = NS_OK;
     if (phase == nsk::PH_GRAM || phase == nsk::PH_A2B) {
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
-      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
+      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n, cl));
       g.cols_valid = static_cast<int>(b.m_pad);
       g.ld_out = static_cast<int>(b.m_pad);
       g.out_stride = b.m_pad * b.m_pad;
@@ -219,7 +237,7 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
       }
     } else {
       g.tiles_n = static_cast<int>((b.n_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
-      g.tiles_per_mat = g.tiles_m * g.tiles_n;
+      g.tiles_per_mat = (cl == 1 ? g.tiles_m : (g.tiles_m + 1) / 2) * g.tiles_n;
       g.cols_valid = static_cast<int>(b.n_pad);
       g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM_BK);
       g.out = nxt;
@@ -250,21 +268,21 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
 int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
               unsigned int* status, cudaStream_t st) {
   nsk::GemmParams gp;
-  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr);
+  const int cl = pick_cl(p, b0, b1, phase);
+  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, cl);
   if (rc != NS_OK) return rc;
-  const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-  return counted(phase, st, [&] { return nsk::launch_gemm(phase, gp, grid, st); }) == cudaSuccess ? NS_OK
-                                                                                           : NS_ERR_CUDA;
+  return counted(phase, st, [&] { return nsk::launch_gemm(phase, cl, gp, nsm, st); }) == cudaSuccess ? NS_OK
+                                                                                             : NS_ERR_CUDA;
 }
 
 // B*X phase of the last step, storing results directly into `out`.
 int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
                  void* const* out, cudaStream_t st) {
   static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
-  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out);
+  const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
+  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, cl);
   if (rc != NS_OK) return rc;
-  const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-  return counted(nsk::PH_BX, st, [&] { return nsk::launch_gemm_final(gp, grid, st); }) == cudaSuccess
+  return counted(nsk::PH_BX, st, [&] { return nsk::launch_gemm_final(cl, gp, nsm, st); }) == cudaSuccess
              ? NS_OK
              : NS_ERR_CUDA;
 }
@@ -714,6 +732,13 @@ int ns_check_status(ns_plan_t* /*plan*/, void* stream) {
     return NS_ERR_DEVICE_CHECK;
   }
   if (cudaGetLastError() != cudaSuccess) return NS_ERR_CUDA;
+  return NS_OK;
+}
+
+int ns_set_gemm_cluster(int cl) {
+  if (cl != 0 && cl != 1 && cl != 2) return NS_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_force_cl = cl;
   return NS_OK;
 }
 

@@ -19,6 +19,8 @@
 // over the padded edge read TMA's zero fill and skip their stores.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -36,31 +38,38 @@ constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 
 constexpr int THREADS = 192;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
 
-template <int PHASE, typename P>
-__device__ __forceinline__ void decode_tile(const P& p, long long t, int& b, int& mat, int& tm, int& tn) {
+// Work item t -> (bucket b, matrix, output tile (tm, tn)). With CL = 2 a work
+// item is a pair of tile rows (2q, 2q + 1) sharing column tile tn; the CTA of
+// cluster rank `rank` takes row 2q + rank. SYRK phases visit only tiles that
+// touch the upper triangle: in tile row tm, column tiles from
+// floor(tm * BM / BN), which is q for both rows of a pair.
+template <int PHASE, int CL, typename P>
+__device__ __forceinline__ void decode_tile(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
+                                            int& tn) {
   b = 0;
   while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
   const GemmBucket& B = p.bk[b];
   const long long local = t - B.tile_begin;
   mat = static_cast<int>(local / B.tiles_per_mat);
   int r = static_cast<int>(local % B.tiles_per_mat);
+  int q;
   if (PHASE == PH_BX) {
-    tm = r / B.tiles_n;
+    q = r / B.tiles_n;
     tn = r % B.tiles_n;
   } else {
-    // upper-triangle tiles: in tile row tm, column tiles from floor(tm*BM/BN)
-    tm = 0;
+    q = 0;
     while (true) {
-      const int tn0 = (tm * BM) / BN;
+      const int tn0 = CL == 1 ? (q * BM) / BN : q;
       const int cnt = B.tiles_n - tn0;
       if (r < cnt) {
         tn = tn0 + r;
         break;
       }
       r -= cnt;
-      ++tm;
+      ++q;
     }
   }
+  tm = CL == 1 ? q : 2 * q + static_cast<int>(rank);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -79,8 +88,14 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& q, float* f) {
 
 // FINAL (B*X phase only): write the cropped, transposed-back result to the
 // caller's tensors listed in p.out_tab instead of the next X buffer.
-template <int PHASE, bool FINAL, typename P>
+// CL = 2: launched as clusters of two CTAs working on tile rows 2q and 2q + 1
+// of the same column tile; each CTA loads its own A tile and half of the
+// shared B tile, multicast to both, so per-SM operand traffic drops from 48 KB
+// to 32 KB per K-block. A stage is refilled only when both CTAs' MMAs have
+// released it (empty barriers count one arrival from each CTA).
+template <int PHASE, bool FINAL, int CL, typename P>
 __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ P p) {
+  static_assert(CL == 1 || CL == 2, "cluster size 1 or 2");
   static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
   constexpr bool B_MN = (PHASE == PH_BX);
   constexpr bool SYRK = (PHASE != PH_BX);
@@ -104,11 +119,15 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   }
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = CL == 1 ? 0u : cluster_ctarank();
+  const long long t0 = CL == 1 ? static_cast<long long>(blockIdx.x) : static_cast<long long>(cluster_id_x());
+  const long long tstride = CL == 1 ? static_cast<long long>(gridDim.x) : static_cast<long long>(cluster_count_x());
+  constexpr uint16_t MC_ALL = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -128,6 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -135,9 +155,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
-      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
@@ -145,13 +165,28 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
         uint8_t* a_dst = sA + stage * A_BYTES;
         uint8_t* b_dst = sB + stage * B_BYTES;
         tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
-        if (!B_MN) {
-          tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
-          tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
-        } else {
+        if (CL == 1) {
+          if (!B_MN) {
+            tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
+            tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
+          }
+        } else {
+          // this CTA's half of the shared B tile, multicast to both CTAs
+          if (!B_MN) {
+            tma_load_3d_mc(b_dst + rank * (128 * 128), &p.tmb[b], &full[stage], kb * BK,
+                           tn * BN + static_cast<int>(rank) * 128, mat, MC_ALL);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < BN / 128; ++jj) {
+              const int j = static_cast<int>(rank) * (BN / 128) + jj;
+              tma_load_3d_mc(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat,
+                             MC_ALL);
+            }
+          }
         }
         ++issued;
         if (++stage == STAGES) {
@@ -170,9 +205,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   } else if (warp == 1 && lane == 0) {
     // ----------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
-      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
       tc_fence_after();
@@ -189,7 +224,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
           mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        mma_commit(&empty[stage]);
+        if (CL == 1)
+          mma_commit(&empty[stage]);
+        else
+          mma_commit_mc(&empty[stage], MC_ALL);  // the stage is free once both CTAs are done with it
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -208,19 +246,22 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     // -------------------------------------------------------------- epilogue
     const int lg = warp & 3;  // this warp may read TMEM lanes [32*lg, 32*lg + 32)
     uint32_t acc = 0, acc_phase = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
-      decode_tile<PHASE>(p, t, b, mat, tm, tn);
+      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
       const GemmBucket& B = p.bk[b];
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
+      // a pair's second row past the last tile row (odd tiles_m): computed on
+      // TMA's zero fill, nothing to store
+      const int cend = tm < B.tiles_m ? BN : 0;
       const int r0w = tm * BM + lg * 32;  // first row of this warp
       const int r = r0w + lane;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(mat) * B.out_stride;
       const __nv_bfloat16* aux =
           reinterpret_cast<const __nv_bfloat16*>(B.aux) + static_cast<long long>(mat) * B.aux_stride;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < cend; c0 += 32) {
         const int cg = tn * BN + c0;
         if (cg >= B.cols_valid) break;          // warp-uniform
         if (SYRK && cg + 31 < r0w) continue;    // chunk entirely below the diagonal for this warp
@@ -313,32 +354,72 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if (CL > 1) {
+    // no CTA leaves while its peer may still multicast into it or arrive on
+    // its barriers
+    __syncwarp();
+    cluster_sync_all();
+  }
 }
 
-template <int PHASE, bool FINAL, typename P>
-cudaError_t launch_one(const P& p, int grid, cudaStream_t st) {
-  auto kern = ns_gemm_kernel<PHASE, FINAL, P>;
+template <int PHASE, bool FINAL, int CL, typename P>
+cudaError_t launch_one(const P& p, int work_items, int nsm, cudaStream_t st) {
+  auto kern = ns_gemm_kernel<PHASE, FINAL, CL, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (CL == 1) {
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min(work_items, nsm)));
+    cfg.numAttrs = 0;
+  } else {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(CL * (nsm / CL)));
+    int max_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(static_cast<unsigned>(CL * std::min(work_items, max_clusters)));
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st) {
-  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+cudaError_t launch_gemm(int phase, int cl, const GemmParams& p, int nsm, cudaStream_t st) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
+  if (cl == 2) {
+    switch (phase) {
+      case PH_GRAM: return launch_one<PH_GRAM, false, 2>(p, items, nsm, st);
+      case PH_A2B: return launch_one<PH_A2B, false, 2>(p, items, nsm, st);
+      case PH_BX: return launch_one<PH_BX, false, 2>(p, items, nsm, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (phase) {
-    case PH_GRAM: return launch_one<PH_GRAM, false>(p, grid, st);
-    case PH_A2B: return launch_one<PH_A2B, false>(p, grid, st);
-    case PH_BX: return launch_one<PH_BX, false>(p, grid, st);
+    case PH_GRAM: return launch_one<PH_GRAM, false, 1>(p, items, nsm, st);
+    case PH_A2B: return launch_one<PH_A2B, false, 1>(p, items, nsm, st);
+    case PH_BX: return launch_one<PH_BX, false, 1>(p, items, nsm, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gemm_final(const GemmFinalParams& p, int grid, cudaStream_t st) {
-  if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-  return launch_one<PH_BX, true>(p, grid, st);
+cudaError_t launch_gemm_final(int cl, const GemmFinalParams& p, int nsm, cudaStream_t st) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
+  if (cl == 2) return launch_one<PH_BX, true, 2>(p, items, nsm, st);
+  return launch_one<PH_BX, true, 1>(p, items, nsm, st);
 }
 
 }  // namespace nsk

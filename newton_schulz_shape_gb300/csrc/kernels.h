@@ -161,8 +161,11 @@ struct PackParams {
 };
 
 // ----------------------------------------------------------------- launchers
-cudaError_t launch_gemm(int phase, const GemmParams& p, int grid, cudaStream_t st);
-cudaError_t launch_gemm_final(const GemmFinalParams& p, int grid, cudaStream_t st);
+// cl = 1: one CTA per tile; cl = 2: clusters of two CTAs sharing the B tile
+// (p.bk[].tiles_per_mat then counts tile-row pairs). The launchers size the
+// grid from the work items, the SM count and cluster occupancy.
+cudaError_t launch_gemm(int phase, int cl, const GemmParams& p, int nsm, cudaStream_t st);
+cudaError_t launch_gemm_final(int cl, const GemmFinalParams& p, int nsm, cudaStream_t st);
 cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st);
 cudaError_t launch_scale(const ProParams& p, cudaStream_t st);
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st);

@@ -96,3 +96,31 @@ def test_repeatable_bitwise():
     b = run_ns(nsg, shapes, ts)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("cl", [0, 1])
+def test_cluster_pairs_odd_tile_rows(cl):
+    # m_pad = 384, 384, 640: odd tile-row counts leave a spare CTA in the last pair
+    shapes = [(300, 700), (700, 300), (640, 960), (256, 256)]
+    ts = workloads.gen_tensors(workloads.Workload("odd", shapes, 0.02, 17))
+    nsg.ns_set_gemm_cluster(cl)
+    try:
+        outs = run_ns(nsg, shapes, ts)
+    finally:
+        nsg.ns_set_gemm_cluster(0)
+    for s_, t, o in zip(shapes, ts, outs):
+        assert rel_err(o, oracle_ns(t)) <= BF16_TOL, (cl, s_)
+
+
+def test_cluster_and_single_cta_agree():
+    shapes = [(1024, 3072), (2048, 1024)]
+    ts = workloads.gen_tensors(workloads.Workload("agree", shapes, 0.02, 18))
+    a = run_ns(nsg, shapes, ts)
+    nsg.ns_set_gemm_cluster(1)
+    try:
+        b = run_ns(nsg, shapes, ts)
+    finally:
+        nsg.ns_set_gemm_cluster(0)
+    for x, y in zip(a, b):
+        # the same products in the same K order: bitwise equal
+        assert torch.equal(x, y)
