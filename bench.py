@@ -41,21 +41,37 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe"], default="gpt")
+    ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe", "sweep"], default="gpt")
+    ap.add_argument("--gram", choices=["bf16", "fp32"], default="bf16",
+                    help="precision policy (sweep workload): bf16 path or fp32-Gram (split TF32) path")
+    ap.add_argument("--ridge", type=float, default=0.0, help="trace ridge (fp32-Gram path only)")
+    ap.add_argument("--points", type=str, default="",
+                    help="sweep subset, e.g. '1024x1,4096x8' (m x aspect); default: all")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
+    ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM tiling: 0 automatic (2-CTA clusters sharing B tiles), 1 single-CTA tiles")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
 
-PER_LAYER = {"gpt": 4, "llama": 5, "moe": 3 * 64, "small": 1}
+PER_LAYER = {"gpt": 4, "llama": 5, "moe": 3 * 64, "small": 1, "sweep": 1}
+
+
+def sweep_workload():
+    import workloads
+    shapes = []
+    for (m, a, bt) in workloads.sweep_points():
+        shapes += [(m, a * m)] * bt
+    shapes += [(256, 64, 3, 3)] * 64
+    return workloads.Workload("size/aspect sweep", shapes, 0.02, 5000, S=1)
 
 
 def get_workload(name: str, layers: int = 0):
     import workloads
     w = {"gpt": workloads.gpt_24l_d2048, "small": workloads.small_16x128x256,
-         "llama": workloads.llama8b_32l, "moe": workloads.moe_16l_64e}[name]()
+         "llama": workloads.llama8b_32l, "moe": workloads.moe_16l_64e, "sweep": sweep_workload}[name]()
     if layers > 0:
         w.shapes = w.shapes[:layers * PER_LAYER[name]]
         w.name += f" (first {layers} layers)"
@@ -183,19 +199,26 @@ class ClockSampler:
 # --------------------------------------------------------------- CPU oracle
 def cpu_oracle_sample(w, budget_s: float = 20.0):
     """Time the float64 oracle on one matrix per shape bucket (and the routing
-    oracle on those tensors), extrapolated to the whole workload by count."""
-    import numpy as np
+    oracle on those tensors), smallest buckets first, until `budget_s` is
+    spent; extrapolate to the whole workload by count, and by useful flops at
+    the sampled rate for buckets not sampled."""
+    import numpy as np  # noqa: F401
     import workloads
     from oracle import ns as ons
     from oracle import routing as orr
     buckets = {}
     for i, s in enumerate(w.shapes):
         buckets.setdefault(view_mn(s), []).append(i)
-    total_est = 0.0
-    sample = []
-    spent = 0.0
-    for (m, n), idx in buckets.items():
+    order = sorted(buckets, key=lambda mn: mn[0] * mn[0] * mn[1])
+    total_est, spent, sampled_flops = 0.0, 0.0, 0
+    sample, unsampled = [], []
+    for mn in order:
+        idx = buckets[mn]
         i = idx[0]
+        fl = sum(flops_by_kind([w.shapes[i]], workloads.STEPS).values())
+        if spent > budget_s:
+            unsampled.append((len(idx), fl))
+            continue
         t = workloads.gen_tensor(w.shapes[i], w.sigma, w.seed, i)
         x = t.float().numpy()
         bits = t.view(__import__("torch").int16).numpy()
@@ -206,10 +229,14 @@ def cpu_oracle_sample(w, budget_s: float = 20.0):
         orr.route_from_ns_home(homes, [w.shapes[i]], {0: 0}, w.S, 0)
         dt = time.perf_counter() - t0
         spent += dt
+        sampled_flops += fl
         total_est += dt * len(idx)
         sample.append(f"{len(idx)}x{tuple(w.shapes[i])}: {dt:.2f}s")
-        if spent > budget_s:
-            break
+    if unsampled:
+        rate = sampled_flops / spent
+        total_est += sum(c * fl / rate for c, fl in unsampled)
+        sample.append(f"{sum(c for c, _ in unsampled)} matrices in {len(unsampled)} larger buckets "
+                      f"extrapolated at the sampled {rate / 1e9:.0f} GFLOP/s")
     try:
         import threadpoolctl
         threads = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
@@ -262,6 +289,7 @@ def run_ours(args):
 
     w = get_workload(args.workload, args.layers)
     w.seed = replica_seed(w.seed, rank, world)
+    nsg.ns_set_gemm_cluster(args.gemm_cluster)
     S, shapes = w.S, w.shapes
     plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=S, shard_dim=0)
     home_off, home_sizes, rank_sizes = plan.home_layout()
@@ -444,7 +472,7 @@ def run_ours(args):
         "data": "synthetic: seeded N(0, sigma) bf16 per tensor (sigma 0.02)",
         "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
                                f"pack -> NS (5 steps) -> unpack",
-                   "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS,
+                   "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS, "gemm_cluster": args.gemm_cluster,
                    "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
         "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
         "ns_only": {"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,
@@ -466,10 +494,81 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ sweep
+def run_sweep(args):
+    """Size/aspect sweep: NS alone (no pack) on each point's batch, one plan
+    per point, inputs resident in HBM; per-point useful TFLOP/s and the whole
+    sweep's matrices/s."""
+    import torch
+
+    import newton_schulz_shape_gb300 as nsg
+    import workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    pts = [(m, a, bt) for (m, a, bt) in workloads.sweep_points()]
+    if args.points:
+        want = {tuple(int(x) for x in p.split("x")) for p in args.points.split(",")}
+        pts = [p for p in pts if (p[0], p[1]) in want]
+    mode = nsg.NS_FP32_GRAM if args.gram == "fp32" else nsg.NS_BF16
+    stream = torch.cuda.current_stream(dev)
+    results, tot_ms, tot_mats, tot_flops = [], 0.0, 0, 0
+    runs = [(f"{m}x{a * m}", [(m, a * m)] * bt, 5000 + m + a) for (m, a, bt) in pts]
+    if not args.points:
+        runs.append(("256x64x3x3", [(256, 64, 3, 3)] * 64, 5999))
+    clocks = ClockSampler("")
+    clocks.start()
+    for name, shapes, seed in runs:
+        w = workloads.Workload(name, shapes, 0.02, seed)
+        ins = [workloads.gen_tensor(s, w.sigma, w.seed, i).to(dev) for i, s in enumerate(shapes)]
+        odt = torch.float32 if mode == nsg.NS_FP32_GRAM else torch.bfloat16
+        outs = [torch.empty(s, dtype=odt, device=dev) for s in shapes]
+        plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, gram_mode=mode,
+                                  ridge=args.ridge, S=1)
+        ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+        for _ in range(max(3, args.warmup)):
+            nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        rc = nsg.ns_check_status(plan, stream)
+        if rc != nsg.NS_OK:
+            raise RuntimeError(f"{name}: {nsg.ns_status_string(rc)}")
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        fl = sum(sum(flops_by_kind([s], workloads.STEPS).values()) for s in shapes)
+        results.append({"point": name, "matrices": len(shapes), "ms": ms,
+                        "tflops_useful": fl / (ms * 1e-3) / 1e12})
+        tot_ms += ms
+        tot_mats += len(shapes)
+        tot_flops += fl
+        del ins, outs, ws, plan
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    burst, sustained, _, src = peaks()
+    line = {"metric": METRIC, "value": tot_mats * 1000.0 / tot_ms, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": tot_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if mode == nsg.NS_BF16 else "f32 (split-TF32 products)",
+            "data": "synthetic: seeded N(0, 0.02) bf16 per tensor",
+            "config": {"workload": "size/aspect sweep: m in {1024..8192} x aspect {1,2,4,8} (+ 256x64x3x3), NS only",
+                       "gram": args.gram, "ridge": args.ridge},
+            "tflops_useful": tot_flops / (tot_ms * 1e-3) / 1e12,
+            "peak_bf16_tflops": {"burst": burst, "sustained": sustained, "source": src},
+            "points": results, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -250,8 +250,6 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       int b, mat, tm, tn;
       decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
       const GemmBucket& B = p.bk[b];
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
       // a pair's second row past the last tile row (odd tiles_m): computed on
       // TMA's zero fill, nothing to store
       const int cend = tm < B.tiles_m ? BN : 0;
@@ -260,8 +258,27 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(mat) * B.out_stride;
       const __nv_bfloat16* aux =
           reinterpret_cast<const __nv_bfloat16*>(B.aux) + static_cast<long long>(mat) * B.aux_stride;
-#pragma unroll 1
-      for (int c0 = 0; c0 < cend; c0 += 32) {
+      // Fetch this thread's row of the aux tile (A or X, 8 chunks of 64 bytes)
+      // into registers before waiting for the accumulator: the loads complete
+      // while the tile's MMAs run instead of stalling the epilogue.
+      uint4 ax[BN / 32][4];
+      if (PHASE != PH_GRAM) {
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          const int cg = tn * BN + ci * 32;
+          if (ci * 32 < cend && cg < B.cols_valid && !(SYRK && cg + 31 < r0w)) {
+            const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<long long>(r) * B.ld_aux + cg);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ax[ci][q] = __ldcg(src + q);
+          }
+        }
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ci = 0; ci < BN / 32; ++ci) {
+        const int c0 = ci * 32;
+        if (c0 >= cend) break;
         const int cg = tn * BN + c0;
         if (cg >= B.cols_valid) break;          // warp-uniform
         if (SYRK && cg + 31 < r0w) continue;    // chunk entirely below the diagonal for this warp
@@ -272,11 +289,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
         if (PHASE != PH_GRAM) {
-          const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<long long>(r) * B.ld_aux + cg);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float x[8];
-            unpack_bf16x8(src[q], x);
+            unpack_bf16x8(ax[ci][q], x);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               if (PHASE == PH_A2B)
