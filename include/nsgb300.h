@@ -218,11 +218,13 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * is enabled, every launch is bracketed by two CUDA events recorded on the
  * stream it is launched on; ns_profile_read synchronises those events. */
 
-/* Tuning: how the bf16 GEMM phases tile the tensor cores. cl = 0 (default)
- * pairs CTAs into 2-CTA clusters that share each B tile by TMA multicast
- * whenever every bucket of a launch has at least two 128-row tile rows;
- * cl = 1 never pairs; cl = 2 behaves like 0. Process-wide; results are the
- * same up to fp32 summation order. */
+/* Tuning: how the bf16 GEMM phases use the tensor cores. cl = 1: one CTA per
+ * 128 x 256 tile (tcgen05 cta_group::1); cl = 2: clusters of two such CTAs
+ * sharing each B tile by TMA multicast; cl = 3: clusters of two CTAs running
+ * the 2-SM MMA (cta_group::2) on 256 x 256 tiles, each SM holding half of
+ * each operand; cl = 0 (default) picks 3. Paired modes apply to launches
+ * whose buckets all have at least two 128-row tile rows; others use 1.
+ * Process-wide; all modes give bitwise-identical results. */
 int ns_set_gemm_cluster(int cl);
 
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */

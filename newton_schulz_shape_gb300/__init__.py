@@ -234,5 +234,5 @@ def ns_profile_read(reset: bool = False):
 
 
 def ns_set_gemm_cluster(cl: int) -> None:
-    """0: pair CTAs into B-sharing clusters when possible (default); 1: never."""
+    """GEMM tiling: 0 automatic (2-SM MMA), 1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")

@@ -40,7 +40,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
-int g_force_cl = 0;  // 0: automatic; 1: never pair CTAs; 2: pair whenever possible
+int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
 
 // ----------------------------------------------------------- measurement
 constexpr int kKinds = 5;
@@ -156,16 +156,21 @@ long long syrk_tiles(int tiles_m, int tiles_n, int cl = 1) {
   return t;
 }
 
-// Cluster size for a launch: pairs of CTAs share B tiles when every bucket of
-// the launch has at least two tile rows.
+// GEMM tiling for a launch: 1 = one CTA per 128 x 256 tile; 2 = CTA pairs
+// sharing B tiles by multicast; 3 = CTA pairs running the 2-SM MMA on
+// 256 x 256 tiles. Pairs need every bucket of the launch to have at least two
+// tile rows; the default is the 2-SM MMA.
 int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   for (size_t bi = b0; bi < b1; ++bi) {
     const Bucket& b = p.buckets[bi];
     if (b.m_pad / nsk::GEMM_BM < 2) return 1;
   }
   (void)phase;
-  return g_force_cl ? g_force_cl : 2;
+  return g_force_cl ? g_force_cl : 3;
 }
+
+// Work items per matrix count tile-row pairs for both paired modes.
+int count_mode(int cl) { return cl == 1 ? 1 : 2; }
 
 struct BucketPtrs {
   char* x0;
@@ -269,10 +274,13 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
               unsigned int* status, cudaStream_t st) {
   nsk::GemmParams gp;
   const int cl = pick_cl(p, b0, b1, phase);
-  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, cl);
+  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl));
   if (rc != NS_OK) return rc;
-  return counted(phase, st, [&] { return nsk::launch_gemm(phase, cl, gp, nsm, st); }) == cudaSuccess ? NS_OK
-                                                                                             : NS_ERR_CUDA;
+  return counted(phase, st, [&] {
+           return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, cl, gp, nsm, st);
+         }) == cudaSuccess
+             ? NS_OK
+             : NS_ERR_CUDA;
 }
 
 // B*X phase of the last step, storing results directly into `out`.
@@ -280,9 +288,11 @@ int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, 
                  void* const* out, cudaStream_t st) {
   static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
   const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
-  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, cl);
+  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl));
   if (rc != NS_OK) return rc;
-  return counted(nsk::PH_BX, st, [&] { return nsk::launch_gemm_final(cl, gp, nsm, st); }) == cudaSuccess
+  return counted(nsk::PH_BX, st, [&] {
+           return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(cl, gp, nsm, st);
+         }) == cudaSuccess
              ? NS_OK
              : NS_ERR_CUDA;
 }
@@ -736,7 +746,7 @@ int ns_check_status(ns_plan_t* /*plan*/, void* stream) {
 }
 
 int ns_set_gemm_cluster(int cl) {
-  if (cl != 0 && cl != 1 && cl != 2) return NS_ERR_ARG;
+  if (cl < 0 || cl > 3) return NS_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_cl = cl;
   return NS_OK;

@@ -1,0 +1,388 @@
+// 2-SM (cta_group::2) form of the three bf16 Newton-Schulz products (see
+// gemm.cu for the phases and their epilogues; Megatron-Core API page
+// owner_planning, ns_cost_fn).
+//
+// A cluster of two CTAs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by one thread of
+// the leader CTA (cluster rank 0). Each CTA holds, per 64-wide K block, only
+// its own half of each operand: A rows [tm*128, +128) with tm = 2q + rank, and
+// B rows (or columns) [tn*256 + rank*128, +128): 32 KB per stage per SM,
+// against 48 KB when one SM holds a whole 128 x 256 tile's operands. The
+// accumulator is split by rows: each CTA's TMEM holds its 128 rows x 256
+// fp32 columns, so each CTA's epilogue works exactly as in the 1-SM kernel.
+//
+// Synchronisation (all waits bounded):
+//   full[s]   leader only; count 2 (leader arrive.expect_tx of both halves'
+//             bytes + the peer's remote arrive); both CTAs' TMA loads signal it
+//   empty[s]  both CTAs; the leader's MMA commit is multicast to both
+//   tfull[a]  both CTAs; the leader's commit after a tile, multicast
+//   tempty[a] leader only; count 8 = 4 epilogue warps x 2 CTAs (remote arrive)
+// TMEM is allocated and freed collectively by one warp in each CTA.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nsk {
+namespace {
+
+using namespace nsptx;
+
+constexpr int BM = GEMM_BM;          // rows per CTA (M = 256 per pair)
+constexpr int BN = GEMM_BN;          // output columns per tile
+constexpr int BK = GEMM_BK, UK = 16;
+constexpr int STAGES = 6;
+constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;   // 16 KB: this CTA's half of B
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+
+template <int PHASE, typename P>
+__device__ __forceinline__ void decode_pair(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
+                                            int& tn) {
+  b = 0;
+  while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
+  const GemmBucket& B = p.bk[b];
+  const long long local = t - B.tile_begin;
+  mat = static_cast<int>(local / B.tiles_per_mat);
+  int r = static_cast<int>(local % B.tiles_per_mat);
+  int q;
+  if (PHASE == PH_BX) {
+    q = r / B.tiles_n;
+    tn = r % B.tiles_n;
+  } else {
+    // 256-row block q touches the upper triangle in column tiles tn >= q
+    q = 0;
+    while (true) {
+      const int cnt = B.tiles_n - q;
+      if (r < cnt) {
+        tn = q + r;
+        break;
+      }
+      r -= cnt;
+      ++q;
+    }
+  }
+  tm = 2 * q + static_cast<int>(rank);
+}
+
+__device__ __forceinline__ uint32_t pack2bf(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& q, float* f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+template <int PHASE, bool FINAL, typename P>
+__global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_constant__ P p) {
+  static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
+  constexpr bool B_MN = (PHASE == PH_BX);
+  constexpr bool SYRK = (PHASE != PH_BX);
+  constexpr uint32_t IDESC = idesc_make(1u, 2 * BM, BN, false, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (blockDim.x != THREADS) {
+    if (threadIdx.x == 0) atomicOr(p.status, NS_DEV_BAD_LAUNCH);
+    return;
+  }
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const long long t0 = static_cast<long long>(cluster_id_x());
+  const long long tstride = static_cast<long long>(cluster_count_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    for (int b = 0; b < p.nb; ++b) {
+      prefetch_tmap(&p.tma[b]);
+      prefetch_tmap(&p.tmb[b]);
+    }
+  }
+  // the collective 2-SM TMEM allocation needs the peer CTA running: meet first
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    long long issued = 0;
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
+      int b, mat, tm, tn;
+      decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
+        const uint32_t full_l = map_to_rank(&full[stage], 0);
+        if (leader)
+          mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
+        else
+          mbar_arrive_cluster(full_l);
+        tma_load_3d_pair(sA + stage * A_BYTES, &p.tma[b], full_l, kb * BK, tm * BM, mat);
+        uint8_t* b_dst = sB + stage * B_BYTES;
+        const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
+        if (!B_MN) {
+          tma_load_3d_pair(b_dst, &p.tmb[b], full_l, kb * BK, n0, mat);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 128; ++j)
+            tma_load_3d_pair(b_dst + j * (64 * 128), &p.tmb[b], full_l, n0 + j * 64, kb * BK, mat);
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    if (*abort_flag && leader) {
+      const long long first = issued > STAGES ? issued - STAGES : 0;
+      for (long long i = first; i < issued; ++i)
+        mbar_wait_drain(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.status);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ----------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
+      int b, mat, tm, tn;
+      decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
+      const int kb_n = p.bk[b].k_blocks;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < kb_n; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto mma_done;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k) {
+          const uint64_t ad = sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+          const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+                                   : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
+          mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit_pair_mc(&empty[stage], 3);  // both CTAs' copies of the stage are free
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit_pair_mc(&tfull[acc], 3);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  mma_done:
+    if (*abort_flag) {
+      mma_commit_pair_mc(drain, 1);
+      mbar_wait_drain(drain, 0, p.status);
+    }
+  } else if (warp >= 2) {
+    // -------------------------------------------------------------- epilogue
+    const int lg = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (long long t = t0; t < p.total_tiles; t += tstride) {
+      int b, mat, tm, tn;
+      decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
+      const GemmBucket& B = p.bk[b];
+      const int cend = tm < B.tiles_m ? BN : 0;  // the spare half of an odd last pair stores nothing
+      const int r0w = tm * BM + lg * 32;
+      const int r = r0w + lane;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(mat) * B.out_stride;
+      const __nv_bfloat16* aux =
+          reinterpret_cast<const __nv_bfloat16*>(B.aux) + static_cast<long long>(mat) * B.aux_stride;
+      uint4 ax[BN / 32][4];
+      if (PHASE != PH_GRAM) {
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          const int cg = tn * BN + ci * 32;
+          if (ci * 32 < cend && cg < B.cols_valid && !(SYRK && cg + 31 < r0w)) {
+            const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<long long>(r) * B.ld_aux + cg);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ax[ci][q] = __ldcg(src + q);
+          }
+        }
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ci = 0; ci < BN / 32; ++ci) {
+        const int c0 = ci * 32;
+        if (c0 >= cend) break;
+        const int cg = tn * BN + c0;
+        if (cg >= B.cols_valid) break;
+        if (SYRK && cg + 31 < r0w) continue;
+        uint32_t v[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + acc * BN + c0, v);
+        tmem_ld_wait();
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (PHASE != PH_GRAM) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float x[8];
+            unpack8(ax[ci][q], x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (PHASE == PH_A2B)
+                f[q * 8 + e] = p.beta * x[e] + p.gamma * f[q * 8 + e];
+              else
+                f[q * 8 + e] = p.alpha * x[e] + f[q * 8 + e];
+            }
+          }
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack2bf(f[2 * j], f[2 * j + 1]);
+        const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(w);
+        if (FINAL) {
+          if (r < B.m_valid) {
+            const unsigned long long e = p.out_tab[B.out_first + mat];
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e & ~1ull);
+            if (!(e & 1ull)) {
+              __nv_bfloat16* dst = o + static_cast<long long>(r) * B.n_valid + cg;
+              if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.n_valid) dst[j] = hv[j];
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (cg + j < B.n_valid) o[static_cast<long long>(cg + j) * B.m_valid + r] = hv[j];
+            }
+          }
+          continue;
+        }
+        __nv_bfloat16* dst = out + static_cast<long long>(r) * B.ld_out + cg;
+        if (!SYRK || cg >= r) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (cg + j >= r) dst[j] = hv[j];
+        }
+        if (SYRK) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = cg + j;
+            if (c > r) out[static_cast<long long>(c) * B.ld_out + r] = hv[j];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs done: no more multicast arrivals or remote arrives
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+  __syncthreads();
+  cluster_sync_all();
+}
+
+template <int PHASE, bool FINAL, typename P>
+cudaError_t launch_pair(const P& p, int work_items, int nsm, cudaStream_t st) {
+  auto kern = ns_gemm2sm_kernel<PHASE, FINAL, P>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (nsm / 2)));
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(work_items, max_clusters)));
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(int phase, const GemmParams& p, int nsm, cudaStream_t st) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
+  switch (phase) {
+    case PH_GRAM: return launch_pair<PH_GRAM, false>(p, items, nsm, st);
+    case PH_A2B: return launch_pair<PH_A2B, false>(p, items, nsm, st);
+    case PH_BX: return launch_pair<PH_BX, false>(p, items, nsm, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_pair_final(const GemmFinalParams& p, int nsm, cudaStream_t st) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
+  return launch_pair<PH_BX, true>(p, items, nsm, st);
+}
+
+}  // namespace nsk
