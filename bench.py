@@ -21,6 +21,8 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+
+import numpy as np
 import json
 import os
 import statistics
@@ -51,6 +53,8 @@ def parse():
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiling: 0 automatic (2-CTA clusters sharing B tiles), 1 single-CTA tiles")
+    ap.add_argument("--split-qkv", action="store_true",
+                    help="orthogonalise Q, K and V blocks of fused QKV projections separately")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -314,11 +318,21 @@ def run_ours(args):
     ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
     ins = [home_in[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
     outs = [home_out[homes[i]].data_ptr() + 2 * home_off[i] for i in range(len(shapes))]
+    ns_shapes = shapes
+    ns_plan = plan
+    if args.split_qkv:
+        # split-QKV: NS over the row blocks of each fused QKV tensor; a row block
+        # of a row-major tensor is contiguous, so its pointer is an offset
+        ns_shapes, parents = workloads.split_rows(shapes)
+        ins = [ins[i] + 2 * r0 * (int(np.prod(shapes[i])) // shapes[i][0]) for i, r0 in parents]
+        outs = [outs[i] + 2 * r0 * (int(np.prod(shapes[i])) // shapes[i][0]) for i, r0 in parents]
+        ns_plan = nsg.ns_plan_create(ns_shapes, steps=workloads.STEPS, eps=workloads.EPS, S=1)
+        ws = torch.empty(ns_plan.workspace_bytes(), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
-        nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        nsg.ns_orthogonalize_batched(ns_plan, ins, outs, ws, stream=stream)
         nsg.ns_unpack_from_home(plan, home_out, rank_out, stream=stream)
 
     for _ in range(max(3, args.warmup)):
@@ -353,7 +367,7 @@ def run_ours(args):
         ev[k][0].record(stream)
         nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
         ev[k][1].record(stream)
-        nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+        nsg.ns_orthogonalize_batched(ns_plan, ins, outs, ws, stream=stream)
         ev[k][2].record(stream)
         nsg.ns_unpack_from_home(plan, home_out, rank_out, stream=stream)
         ev[k][3].record(stream)
@@ -370,7 +384,7 @@ def run_ours(args):
     pack_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     ns_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     unpack_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
-    n_mats = len(shapes)
+    n_mats = len(ns_shapes)
     value = job_value(n_mats, world, ms_step)
 
     # ---- raw copy bandwidth (context for e2e)
@@ -415,7 +429,7 @@ def run_ours(args):
                 if k >= 2:
                     stream.wait_event(ev_out[b])       # rank_out[b] was copied out by step k-2
                 nsg.ns_pack_to_home(plan, rin[b], home_in, stream=stream)
-                nsg.ns_orthogonalize_batched(plan, ins, outs, ws, stream=stream)
+                nsg.ns_orthogonalize_batched(ns_plan, ins, outs, ws, stream=stream)
                 nsg.ns_unpack_from_home(plan, home_out, rout[b], stream=stream)
                 ev_cmp[b].record(stream)
                 with torch.cuda.stream(s_out):
@@ -447,7 +461,7 @@ def run_ours(args):
 
     # ---- roofline of the dominant kernel
     burst, sustained, hbm, peak_src = peaks()
-    fl = flops_by_kind(shapes, workloads.STEPS)
+    fl = flops_by_kind(ns_shapes, workloads.STEPS)
     gemm_kinds = ["gram", "a2b", "bx"]
     dom = max(gemm_kinds, key=lambda k: kms.get(k, 0.0))
     per_launch_ms = kms[dom] / max(1, launches[dom])
@@ -473,6 +487,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
                                f"pack -> NS (5 steps) -> unpack",
                    "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS, "gemm_cluster": args.gemm_cluster,
+                   "split_qkv": bool(args.split_qkv),
                    "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
         "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
         "ns_only": {"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,

@@ -234,5 +234,5 @@ def ns_profile_read(reset: bool = False):
 
 
 def ns_set_gemm_cluster(cl: int) -> None:
-    """GEMM tiling: 0 automatic (2-SM MMA), 1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
+    """GEMM tiling: 0 automatic (single CTA), 1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")

@@ -159,14 +159,15 @@ long long syrk_tiles(int tiles_m, int tiles_n, int cl = 1) {
 // GEMM tiling for a launch: 1 = one CTA per 128 x 256 tile; 2 = CTA pairs
 // sharing B tiles by multicast; 3 = CTA pairs running the 2-SM MMA on
 // 256 x 256 tiles. Pairs need every bucket of the launch to have at least two
-// tile rows; the default is the 2-SM MMA.
+// tile rows. The default is 1: on the measured workloads neither paired mode
+// is faster (see the GEMM profile summaries).
 int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   for (size_t bi = b0; bi < b1; ++bi) {
     const Bucket& b = p.buckets[bi];
     if (b.m_pad / nsk::GEMM_BM < 2) return 1;
   }
   (void)phase;
-  return g_force_cl ? g_force_cl : 3;
+  return g_force_cl ? g_force_cl : 1;
 }
 
 // Work items per matrix count tile-row pairs for both paired modes.

@@ -118,3 +118,29 @@ def gen_random_shapes(n: int, seed: int, max_dim: int = 300, S: int = 1,
                 for _ in range(nd - 1)]
         shapes.append(tuple([first] + rest))
     return shapes
+
+
+# Row splits of fused QKV projections (split-QKV): Q rows, then K, then V.
+QKV_SPLITS = {
+    (6144, 2048): (2048, 2048, 2048),   # GPT-style MHA, d = 2048
+    (6144, 4096): (4096, 1024, 1024),   # Llama-8B GQA: 32 query heads, 8 KV heads, head dim 128
+}
+
+
+def split_rows(shapes, splits=None):
+    """Expand each tensor whose shape has a row split into its row blocks.
+    Returns (block_shapes, parents) with parents[j] = (tensor index, first row)."""
+    splits = QKV_SPLITS if splits is None else splits
+    out, parents = [], []
+    for i, s in enumerate(shapes):
+        sp = splits.get(tuple(s))
+        if sp is None:
+            out.append(tuple(s))
+            parents.append((i, 0))
+            continue
+        r0 = 0
+        for rows in sp:
+            out.append((rows,) + tuple(s[1:]))
+            parents.append((i, r0))
+            r0 += rows
+    return out, parents
