@@ -51,8 +51,8 @@ def parse():
                     help="sweep subset, e.g. '1024x1,4096x8' (m x aspect); default: all")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
-    ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2],
-                    help="GEMM tiling: 0 automatic (2-CTA clusters sharing B tiles), 1 single-CTA tiles")
+    ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="GEMM tiling: 0 automatic, 1 single CTA, 2 multicast CTA pairs, 3 2-SM MMA")
     ap.add_argument("--split-qkv", action="store_true",
                     help="orthogonalise Q, K and V blocks of fused QKV projections separately")
     ap.add_argument("--no-e2e", action="store_true")
