@@ -12,8 +12,11 @@
 // fp32 columns, so each CTA's epilogue works exactly as in the 1-SM kernel.
 //
 // Synchronisation (all waits bounded):
-//   full[s]   leader only; count 2 (leader arrive.expect_tx of both halves'
-//             bytes + the peer's remote arrive); both CTAs' TMA loads signal it
+//   full[s]   leader only; count 1 (the leader's arrive.expect_tx of both
+//             halves' bytes); both CTAs' TMA loads signal it with complete_tx.
+//             The peer's bytes for a phase can only be issued after the
+//             leader's MMA released the previous phase, so they never land in
+//             the wrong phase; the peer needs no arrive (and no fence).
 //   empty[s]  both CTAs; the leader's MMA commit is multicast to both
 //   tfull[a]  both CTAs; the leader's commit after a tile, multicast
 //   tempty[a] leader only; count 8 = 4 epilogue warps x 2 CTAs (remote arrive)
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -156,10 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
         const uint32_t full_l = map_to_rank(&full[stage], 0);
-        if (leader)
-          mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
-        else
-          mbar_arrive_cluster(full_l);
+        if (leader) mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
         tma_load_3d_pair(sA + stage * A_BYTES, &p.tma[b], full_l, kb * BK, tm * BM, mat);
         uint8_t* b_dst = sB + stage * B_BYTES;
         const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);

@@ -309,3 +309,77 @@ def flat_unpack_from_owner(home_buffers, rank_buffers_before, offsets, numels,
             pos += numels[i]
     per = size // S
     return [flat[r * per:(r + 1) * per] for r in range(S)]
+
+
+# --------------------------------------------------- two-stage (GTP_remat x TP)
+#
+# Megatron-Core API page core.optimizer.layer_sharded_a2a: the exchange runs
+# in two stages, first over the GTP_remat group along dim 0, then over the TP
+# group along the param's partition_dim; the Megatron-LM issue #6720 reports
+# fusing the two into one exchange. Model: R remat ranks x T TP ranks, rank
+# rho = r * T + t. TP shard t of a param is slice t of T along partition_dim;
+# rank (r, t) holds slice r of R along dim 0 of that TP shard. The home of a
+# param is one of the R * T ranks.
+
+def two_stage_piece(x: np.ndarray, r: int, t: int, R: int, T: int, pdim: int) -> np.ndarray:
+    """Rank (r, t)'s piece: TP slice t along pdim, then remat slice r along dim 0."""
+    tp = shard_of(x, t, T, pdim)
+    return shard_of(tp, r, R, 0)
+
+
+def make_rank_buffers_two_stage(tensors, R: int, T: int, pdims) -> list[np.ndarray]:
+    out = []
+    for r in range(R):
+        for t in range(T):
+            parts = [np.ascontiguousarray(two_stage_piece(x, r, t, R, T, pd)).reshape(-1)
+                     for x, pd in zip(tensors, pdims)]
+            out.append(np.concatenate(parts) if parts else np.zeros(0, np.uint16))
+    return out
+
+
+def route_two_stage(rank_buffers, shapes, pdims, home_of: dict, R: int, T: int) -> list[np.ndarray]:
+    """The two exchanges done literally: stage 1 gathers, inside each TP rank's
+    remat group, the dim-0 slices of every param onto the remat coordinate of
+    its home (concatenation along dim 0 rebuilds the TP shard); stage 2
+    gathers, inside the home's TP group, the TP shards onto the home
+    (concatenation along partition_dim). Returns the R*T home buffers."""
+    n = len(shapes)
+    S = R * T
+    # cut every rank buffer into pieces
+    pieces = {}
+    for r in range(R):
+        for t in range(T):
+            buf = rank_buffers[r * T + t]
+            pos = 0
+            for i, shp in enumerate(shapes):
+                shp_t = list(shp)
+                shp_t[pdims[i]] //= T
+                shp_p = list(shp_t)
+                shp_p[0] //= R
+                cnt = _numel(shp_p)
+                pieces[(i, r, t)] = buf[pos:pos + cnt].reshape(shp_p)
+                pos += cnt
+    # stage 1: remat group of TP rank t gathers along dim 0
+    tp_shards = {}
+    for i in range(n):
+        for t in range(T):
+            tp_shards[(i, t)] = np.concatenate([pieces[(i, r, t)] for r in range(R)], axis=0)
+    # stage 2: the home's TP group gathers along partition_dim
+    full = [np.concatenate([tp_shards[(i, t)] for t in range(T)], axis=pdims[i]) for i in range(n)]
+    homes = params_by_home(n, home_of, S)
+    return [np.concatenate([full[i].reshape(-1) for i in homes[h]]) if homes[h]
+            else np.zeros(0, rank_buffers[0].dtype) for h in range(S)]
+
+
+def route_two_stage_back(home_buffers, shapes, pdims, home_of: dict, R: int, T: int) -> list[np.ndarray]:
+    """Inverse of route_two_stage: every rank gets its piece of every result."""
+    n = len(shapes)
+    homes = params_by_home(n, home_of, R * T)
+    full = [None] * n
+    for h in range(R * T):
+        pos = 0
+        for i in homes[h]:
+            cnt = _numel(shapes[i])
+            full[i] = home_buffers[h][pos:pos + cnt].reshape(shapes[i])
+            pos += cnt
+    return make_rank_buffers_two_stage(full, R, T, pdims)

@@ -206,3 +206,52 @@ def test_row_shard_bf16_bits_roundtrip():
 def test_row_shard_not_divisible():
     with pytest.raises(ValueError):
         orr.make_rank_buffers([np.zeros((5, 2))], 2, 0)
+
+
+# ------------------------------------------------------- two-stage exchange
+
+def _ts_tensors(shapes, seed=0):
+    g = np.random.default_rng(seed)
+    return [g.integers(0, 60000, size=s).astype(np.uint16) for s in shapes]
+
+
+def test_two_stage_with_one_tp_rank_is_the_row_shard_route():
+    shapes = [(12, 6), (24, 4), (6, 6, 2)]
+    ts = _ts_tensors(shapes)
+    home_of = {0: 2, 1: 0, 2: 1}
+    R = 3
+    two = orr.route_two_stage(orr.make_rank_buffers_two_stage(ts, R, 1, [1, 1, 2]), shapes, [1, 1, 2],
+                              home_of, R, 1)
+    one = orr.route_to_ns_home(orr.make_rank_buffers(ts, R, 0), shapes, home_of, R, 0)
+    for a, b in zip(two, one):
+        assert np.array_equal(a, b)
+
+
+def test_two_stage_with_one_remat_rank_is_a_partition_dim_route():
+    shapes = [(4, 12), (6, 6), (2, 6, 4)]
+    ts = _ts_tensors(shapes, 1)
+    home_of = {0: 1, 1: 1, 2: 0}
+    T = 2
+    pd = [1, 1, 1]
+    two = orr.route_two_stage(orr.make_rank_buffers_two_stage(ts, 1, T, pd), shapes, pd, home_of, 1, T)
+    one = orr.route_to_ns_home(orr.make_rank_buffers(ts, T, 1), shapes, home_of, T, 1)
+    for a, b in zip(two, one):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("R,T", [(2, 2), (2, 4), (3, 2)])
+def test_two_stage_homes_hold_complete_tensors_and_back(R, T):
+    shapes = [(24, 8), (12, 16, 4), (48, 4), (24, 4, 4)]
+    pd = [1, 2, 0, 1]
+    ts = _ts_tensors(shapes, 2)
+    S = R * T
+    home_of = {i: (3 * i + 1) % S for i in range(len(shapes))}
+    ranks = orr.make_rank_buffers_two_stage(ts, R, T, pd)
+    homes = orr.route_two_stage(ranks, shapes, pd, home_of, R, T)
+    for h in range(S):
+        mine = [i for i in range(len(shapes)) if home_of[i] == h]
+        want = np.concatenate([ts[i].reshape(-1) for i in mine]) if mine else np.zeros(0, np.uint16)
+        assert np.array_equal(homes[h], want)
+    back = orr.route_two_stage_back(homes, shapes, pd, home_of, R, T)
+    for a, b in zip(back, ranks):
+        assert np.array_equal(a, b)
