@@ -56,7 +56,8 @@ enum {
 /* Data model of a plan. */
 enum {
   NS_LAYOUT_ROW_SHARD = 0, /* [LSA] every rank holds a (P/S, Q) slice of every param    */
-  NS_LAYOUT_FLAT = 1       /* [OP]  one flat buffer split evenly into S rank ranges     */
+  NS_LAYOUT_FLAT = 1,      /* [OP]  one flat buffer split evenly into S rank ranges     */
+  NS_LAYOUT_TWO_STAGE = 2  /* [LSA] GTP_remat (dim 0) x TP (partition_dim) shards, one fused gather */
 };
 
 typedef struct ns_plan ns_plan_t; /* opaque; owned by the library */
@@ -94,6 +95,21 @@ int ns_assign_owner_work(int n_tensors, const int64_t* costs, const int32_t* can
 int ns_plan_create(int n_tensors, const int32_t* ndims, const int64_t* shapes_flat, int steps,
                    float a, float b, float c, float eps, int gram_mode, float ridge, int S,
                    int shard_dim, const int32_t* home_of, ns_plan_t** plan_out);
+
+/* [LSA] two-stage exchange (GTP_remat group along dim 0, then TP group along
+ * partition_dim) and [ISS] its fusion into one exchange. S = R * T simulated
+ * ranks, rank r*T + t holding remat slice r (along dim 0, of R) of TP slice t
+ * (along partition_dims[i], of T) of every param, params in index order.
+ * ns_pack_to_home assembles each param on its home in ONE gather, equal bit
+ * for bit to running the two stages one after the other; ns_unpack_from_home
+ * is its inverse. partition_dims[i] = 0 needs shape[0] % (R*T) == 0; else
+ * shape[0] % R == 0 and shape[partition_dim] % T == 0 (NS_ERR_NOT_DIVISIBLE).
+ * home_of in [0, R*T) or NULL for LPT homes. Other arguments as in
+ * ns_plan_create. No CUDA call. */
+int ns_plan_create_two_stage(int n_tensors, const int32_t* ndims, const int64_t* shapes_flat,
+                             const int32_t* partition_dims, int R, int T, int steps, float a, float b,
+                             float c, float eps, int gram_mode, float ridge, const int32_t* home_of,
+                             ns_plan_t** plan_out);
 
 /* [OP] GroupOwnerLayout / OwnerGatherPlan data model. Flat-buffer plan: tensor
  * i occupies elements [offsets[i], offsets[i] + numel_i) of a buffer of
@@ -222,7 +238,8 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * 128 x 256 tile (tcgen05 cta_group::1); cl = 2: clusters of two such CTAs
  * sharing each B tile by TMA multicast; cl = 3: clusters of two CTAs running
  * the 2-SM MMA (cta_group::2) on 256 x 256 tiles, each SM holding half of
- * each operand; cl = 0 (default) picks 1, the fastest measured mode. Paired modes apply to launches
+ * each operand; cl = 0 (default) picks 3 for the Gram and B*X phases and 1
+ * for A*A (the fastest measured per phase). Paired modes apply to launches
  * whose buckets all have at least two 128-row tile rows; others use 1.
  * Process-wide; all modes give bitwise-identical results. */
 int ns_set_gemm_cluster(int cl);

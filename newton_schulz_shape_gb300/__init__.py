@@ -16,7 +16,7 @@ import ctypes
 
 from ._lib import (NS_BF16, NS_ERR_ARG, NS_ERR_CUDA, NS_ERR_DEVICE_CHECK, NS_ERR_HOME,  # noqa: F401
                    NS_ERR_NOT_DIVISIBLE, NS_ERR_SHAPE, NS_ERR_TIMEOUT, NS_ERR_UNSUPPORTED,
-                   NS_ERR_WORKSPACE, NS_FP32_GRAM, NS_LAYOUT_FLAT, NS_LAYOUT_ROW_SHARD, NS_OK,
+                   NS_ERR_WORKSPACE, NS_FP32_GRAM, NS_LAYOUT_FLAT, NS_LAYOUT_ROW_SHARD, NS_LAYOUT_TWO_STAGE, NS_OK,
                    LIB_PATH, NsError, check, header_symbols, i32_array, i64_array, lib, ptr_array)
 
 A_COEF, B_COEF, C_COEF = 3.4445, -4.7750, 2.0315
@@ -150,6 +150,20 @@ def ns_plan_create(shapes, steps: int = 5, a: float = A_COEF, b: float = B_COEF,
     return plan
 
 
+def ns_plan_create_two_stage(shapes, partition_dims, R: int, T: int, steps: int = 5, a: float = A_COEF,
+                             b: float = B_COEF, c: float = C_COEF, eps: float = 1e-7, gram_mode: int = NS_BF16,
+                             ridge: float = 0.0, home_of=None) -> NsPlan:
+    """Two-stage (GTP_remat x TP) plan (layer_sharded_a2a), fused into one gather."""
+    nd, sh = _shape_args(shapes)
+    h = ctypes.c_void_p()
+    homes = i32_array(home_of) if home_of is not None else None
+    check(lib.ns_plan_create_two_stage(len(shapes), nd, sh, i32_array(partition_dims), R, T, steps, a, b, c, eps,
+                                       gram_mode, ridge, homes, ctypes.byref(h)), "ns_plan_create_two_stage")
+    plan = NsPlan(h, len(shapes), R * T)
+    plan.shard_dim = 0
+    return plan
+
+
 def ns_plan_create_flat(shapes, offsets, buffer_size: int, participating=None, steps: int = 5,
                         a: float = A_COEF, b: float = B_COEF, c: float = C_COEF, eps: float = 1e-7,
                         gram_mode: int = NS_BF16, ridge: float = 0.0, S: int = 1, owner_of=None) -> NsPlan:
@@ -196,14 +210,14 @@ def ns_orthogonalize_batched_fixed_ws(plan: NsPlan, ins, outs, stream=None) -> N
 
 def ns_pack_to_home(plan: NsPlan, rank_bufs, home_bufs, shard_dim=None, stream=None) -> None:
     """route_to_ns_home / OwnerGatherPlan: S rank buffers -> S home buffers."""
-    sd = 0 if plan.layout == NS_LAYOUT_FLAT else (shard_dim if shard_dim is not None else _plan_shard_dim(plan))
+    sd = 0 if plan.layout != NS_LAYOUT_ROW_SHARD else (shard_dim if shard_dim is not None else _plan_shard_dim(plan))
     check(lib.ns_pack_to_home(plan.handle, ptr_array([_addr(t) for t in rank_bufs]), len(rank_bufs), sd,
                               ptr_array([_addr(t) for t in home_bufs]), _stream(stream)), "ns_pack_to_home")
 
 
 def ns_unpack_from_home(plan: NsPlan, home_bufs, rank_bufs, shard_dim=None, stream=None) -> None:
     """route_from_ns_home / OwnerScatterPlan: S home buffers -> S rank buffers."""
-    sd = 0 if plan.layout == NS_LAYOUT_FLAT else (shard_dim if shard_dim is not None else _plan_shard_dim(plan))
+    sd = 0 if plan.layout != NS_LAYOUT_ROW_SHARD else (shard_dim if shard_dim is not None else _plan_shard_dim(plan))
     check(lib.ns_unpack_from_home(plan.handle, ptr_array([_addr(t) for t in home_bufs]), len(home_bufs), sd,
                                   ptr_array([_addr(t) for t in rank_bufs]), _stream(stream)), "ns_unpack_from_home")
 
@@ -234,5 +248,6 @@ def ns_profile_read(reset: bool = False):
 
 
 def ns_set_gemm_cluster(cl: int) -> None:
-    """GEMM tiling: 0 automatic (single CTA), 1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
+    """GEMM tiling: 0 automatic (2-SM MMA for Gram and B*X, single CTA for A*A),
+    1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")

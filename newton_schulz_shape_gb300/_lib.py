@@ -29,6 +29,7 @@ NS_BF16 = 0
 NS_FP32_GRAM = 1
 NS_LAYOUT_ROW_SHARD = 0
 NS_LAYOUT_FLAT = 1
+NS_LAYOUT_TWO_STAGE = 2
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
@@ -47,6 +48,10 @@ _SIGS = {
                                            ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int, ctypes.c_float, ctypes.c_int, _i32p,
                                            ctypes.POINTER(_planp)]),
+    "ns_plan_create_two_stage": (ctypes.c_int, [ctypes.c_int, _i32p, _i64p, _i32p, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                ctypes.c_float, ctypes.c_int, ctypes.c_float, _i32p,
+                                                ctypes.POINTER(_planp)]),
     "ns_plan_destroy": (ctypes.c_int, [_planp]),
     "ns_plan_info": (ctypes.c_int, [_planp, _i64p]),
     "ns_plan_homes": (ctypes.c_int, [_planp, _i32p]),

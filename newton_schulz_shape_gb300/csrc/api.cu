@@ -159,15 +159,16 @@ long long syrk_tiles(int tiles_m, int tiles_n, int cl = 1) {
 // GEMM tiling for a launch: 1 = one CTA per 128 x 256 tile; 2 = CTA pairs
 // sharing B tiles by multicast; 3 = CTA pairs running the 2-SM MMA on
 // 256 x 256 tiles. Pairs need every bucket of the launch to have at least two
-// tile rows. The default is 1: on the measured workloads neither paired mode
-// is faster (see the GEMM profile summaries).
+// tile rows.
 int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   for (size_t bi = b0; bi < b1; ++bi) {
     const Bucket& b = p.buckets[bi];
     if (b.m_pad / nsk::GEMM_BM < 2) return 1;
   }
-  (void)phase;
-  return g_force_cl ? g_force_cl : 1;
+  if (g_force_cl) return g_force_cl;
+  // measured on the GPT-style workload: the 2-SM MMA is faster for the Gram
+  // (K = n) and B*X phases, single-CTA tiles for A*A (K = m, short tiles)
+  return phase == nsk::PH_A2B ? 1 : 3;
 }
 
 // Work items per matrix count tile-row pairs for both paired modes.
@@ -350,6 +351,7 @@ int route(ns_plan_t* plan, void* const* rank_bufs, void* const* home_bufs, int S
   pp.rank_len = p.rank_len;
   pp.chunk = 32768;
   pp.S = S;
+  pp.T = p.layout == NS_LAYOUT_TWO_STAGE ? p.T : 1;
   pp.flat = p.layout == NS_LAYOUT_FLAT ? 1 : 0;
   pp.elem_bytes = elem_bytes;
   pp.to_home = to_home ? 1 : 0;

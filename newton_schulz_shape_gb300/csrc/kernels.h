@@ -140,8 +140,10 @@ struct RouteEntry {
   long long seg_begin;  // first position of the tensor in the rank coordinate space
   long long seg_len;    // positions it occupies there
   long long home_off;   // element offset of the complete tensor in its home buffer
-  long long inner;      // row-shard: contiguous run inside a shard (D/S * post)
-  long long outer;      // row-shard: stride between runs in the full tensor (D * post)
+  long long inner;      // sharded models: contiguous run inside a rank's piece
+  long long outer;      // sharded models: stride between runs in the full tensor
+  long long mr, mt;     // sharded models: rank rho = r * T + t starts its piece at
+                        // r * mr + t * mt of the full tensor (row-shard: T = 1)
   int home;
   int pad;
 };
@@ -154,7 +156,8 @@ struct PackParams {
   long long rank_len;   // positions per rank buffer
   long long chunk;      // positions per CTA
   int S;
-  int flat;             // 1: flat-buffer model, 0: row-shard model
+  int T;                // TP ranks of the two-stage model (1 otherwise)
+  int flat;             // 1: flat-buffer model, 0: row-shard / two-stage model
   int elem_bytes;       // 2 or 4
   int to_home;          // 1: pack (rank -> home), 0: unpack (home -> rank)
   unsigned int* status;

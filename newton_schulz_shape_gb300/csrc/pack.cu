@@ -8,6 +8,11 @@
 // has, on rank r, `pre` runs of (D/S)*post elements; run u lands at
 // u*D*post + r*(D/S)*post of the complete param.
 //
+// Two-stage model (same page: a GTP_remat stage along dim 0, then a TP stage
+// along partition_dim; fused into one gather here): rank r*T + t holds remat
+// slice r of TP slice t; its piece is again a sequence of runs, run u landing
+// at u*outer + r*mr + t*mt of the complete param.
+//
 // Flat model (page owner_planning, OwnerGatherPlan / OwnerScatterPlan): rank r
 // holds elements [r*size/S, (r+1)*size/S) of one flat buffer; tensor i is
 // [off_i, off_i + numel_i) of that buffer and goes whole to its owner.
@@ -109,10 +114,11 @@ __global__ void __launch_bounds__(PACK_THREADS) ns_pack_kernel(const __grid_cons
       else
         copy_run(rp, hp, (q1 - q0) * eb);
     } else {
+      const long long rbase = static_cast<long long>(r / p.T) * e.mr + static_cast<long long>(r % p.T) * e.mt;
       for (long long u = q0 / e.inner; u * e.inner < q1; ++u) {
         const long long a = max(q0, u * e.inner), b = min(q1, (u + 1) * e.inner);
         char* rp = rank_buf + (e.seg_begin + a) * eb;
-        char* hp = home_buf + (e.home_off + u * e.outer + r * e.inner + (a - u * e.inner)) * eb;
+        char* hp = home_buf + (e.home_off + u * e.outer + rbase + (a - u * e.inner)) * eb;
         if (p.to_home)
           copy_run(hp, rp, (b - a) * eb);
         else

@@ -28,6 +28,8 @@ struct Tensor {
   int bucket = -1, slot = -1;
   // row-shard routing: tensor viewed as (pre, D, post), shard_dim = D
   int64_t pre = 1, D = 1, post = 1, shard_len = 0, rank_off = 0;
+  // sharded models: run length, run stride and rank bases of a piece
+  int64_t run = 0, stride = 0, mr = 0, mt = 0;
   // flat routing
   int64_t flat_off = 0;
 };
@@ -43,6 +45,7 @@ struct Bucket {
 
 struct Plan {
   int layout = 0, S = 1, shard_dim = 0, steps = 5, gram_mode = 0;
+  int R = 1, T = 1;         // two-stage model: GTP_remat x TP ranks (S = R * T)
   float a = 0, b = 0, c = 0, eps = 0, ridge = 0;
   int64_t buffer_size = 0;  // flat model
   int64_t rank_len = 0;     // elements per rank buffer
@@ -62,6 +65,8 @@ constexpr int64_t kSumsqChunk = 32768;
 
 int build_row_shard(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, int S, int shard_dim,
                     const int32_t* home_of);
+int build_two_stage(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, const int32_t* pdims, int R,
+                    int T, const int32_t* home_of);
 int build_flat(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, const int64_t* offsets,
                int64_t size, const uint8_t* participating, int S, const int32_t* owner_of);
 int lpt_assign(int n, const int64_t* costs, const int32_t* cand_ptr, const int32_t* cand_idx, int n_ranks,

@@ -146,12 +146,14 @@ int finish(Plan& p) {
     nsk::RouteEntry e{};
     e.home = t.home;
     e.home_off = t.home_off;
-    if (p.layout == NS_LAYOUT_ROW_SHARD) {
+    if (p.layout != NS_LAYOUT_FLAT) {
       if (t.shard_len == 0) continue;
       e.seg_begin = t.rank_off;
       e.seg_len = t.shard_len;
-      e.inner = (t.D / p.S) * t.post;
-      e.outer = t.D * t.post;
+      e.inner = t.run;
+      e.outer = t.stride;
+      e.mr = t.mr;
+      e.mt = t.mt;
     } else {
       if (t.numel == 0) continue;
       e.seg_begin = t.flat_off;
@@ -201,6 +203,8 @@ int lpt_assign(int n, const int64_t* costs, const int32_t* cand_ptr, const int32
   return NS_OK;
 }
 
+int assign_homes_all(Plan& p, int n, int S, const int32_t* home_of);
+
 int build_row_shard(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, int S, int shard_dim,
                     const int32_t* home_of) {
   p.layout = NS_LAYOUT_ROW_SHARD;
@@ -221,9 +225,20 @@ int build_row_shard(Plan& p, int n, const int32_t* ndims, const int64_t* shapes,
     t.shard_len = t.numel / S;
     t.rank_off = pos;
     pos += t.shard_len;
+    t.run = (t.D / S) * t.post;
+    t.stride = t.D * t.post;
+    t.mr = t.run;
+    t.mt = 0;
     t.participating = true;
   }
   p.rank_len = pos;
+  return assign_homes_all(p, n, S, home_of);
+}
+
+// Homes for the sharded models: explicit, or LPT with every rank a candidate
+// (every rank holds a piece of every param).
+int assign_homes_all(Plan& p, int n, int S, const int32_t* home_of) {
+  int rc;
   if (home_of) {
     for (int i = 0; i < n; ++i) {
       if (home_of[i] < 0 || home_of[i] >= S) return NS_ERR_HOME;
@@ -245,6 +260,54 @@ int build_row_shard(Plan& p, int n, const int32_t* ndims, const int64_t* shapes,
     for (int i = 0; i < n; ++i) p.t[i].home = own[i];
   }
   return finish(p);
+}
+
+int build_two_stage(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, const int32_t* pdims, int R,
+                    int T, const int32_t* home_of) {
+  p.layout = NS_LAYOUT_TWO_STAGE;
+  p.R = R;
+  p.T = T;
+  p.S = R * T;
+  p.shard_dim = 0;
+  int rc = load_tensors(p, n, ndims, shapes, false);
+  if (rc != NS_OK) return rc;
+  int64_t pos = 0;
+  for (int i = 0; i < n; ++i) {
+    Tensor& t = p.t[i];
+    const int d = pdims[i];
+    if (d < 0 || d >= t.ndim) return NS_ERR_ARG;
+    const int64_t P = t.shape[0];
+    int64_t pre = 1;  // dims strictly between 0 and d
+    for (int k = 1; k < d; ++k) pre *= t.shape[k];
+    const int64_t D = t.shape[d];
+    int64_t post = 1;
+    for (int k = d + 1; k < t.ndim; ++k) post *= t.shape[k];
+    t.shard_len = t.numel / (int64_t(R) * T);
+    if (d == 0) {
+      // both stages split dim 0: TP slice t of P/T rows, remat slice r of it;
+      // the piece of rank (r, t) is one contiguous block of rows
+      if (P % (int64_t(R) * T)) return NS_ERR_NOT_DIVISIBLE;
+      t.run = t.shard_len;
+      t.stride = t.shard_len;
+      t.mr = t.shard_len;
+      t.mt = int64_t(R) * t.shard_len;
+    } else {
+      // TP slice t: columns [t*D/T, (t+1)*D/T) of dim d; remat slice r: rows
+      // [r*P/R, (r+1)*P/R). Runs of (D/T)*post elements, one per (row, pre).
+      if (P % R || D % T) return NS_ERR_NOT_DIVISIBLE;
+      const int64_t cols = t.numel / std::max<int64_t>(P, 1);  // prod(shape[1:])
+      t.run = (D / T) * post;
+      t.stride = D * post;
+      t.mr = (P / R) * cols;
+      t.mt = (D / T) * post;
+      (void)pre;
+    }
+    t.rank_off = pos;
+    pos += t.shard_len;
+    t.participating = true;
+  }
+  p.rank_len = pos;
+  return assign_homes_all(p, n, p.S, home_of);
 }
 
 namespace {
@@ -418,6 +481,34 @@ int ns_plan_create(int n_tensors, const int32_t* ndims, const int64_t* shapes_fl
   p.gram_mode = gram_mode;
   p.ridge = ridge;
   rc = nsplan::build_row_shard(p, n_tensors, ndims, shapes_flat, S, shard_dim, home_of);
+  if (rc != NS_OK) {
+    delete pl;
+    return rc;
+  }
+  *plan_out = pl;
+  return NS_OK;
+}
+
+int ns_plan_create_two_stage(int n_tensors, const int32_t* ndims, const int64_t* shapes_flat,
+                             const int32_t* partition_dims, int R, int T, int steps, float a, float b, float c,
+                             float eps, int gram_mode, float ridge, const int32_t* home_of, ns_plan_t** plan_out) {
+  if (!plan_out) return NS_ERR_ARG;
+  *plan_out = nullptr;
+  if (n_tensors < 0 || (n_tensors > 0 && (!ndims || !shapes_flat || !partition_dims))) return NS_ERR_ARG;
+  if (R < 1 || T < 1 || int64_t(R) * T > nsplan::kMaxRanks) return NS_ERR_ARG;
+  int rc = check_coeffs(steps, eps, gram_mode, ridge);
+  if (rc != NS_OK) return rc;
+  ns_plan* pl = new (std::nothrow) ns_plan();
+  if (!pl) return NS_ERR_ARG;
+  Plan& p = pl->p;
+  p.steps = steps;
+  p.a = a;
+  p.b = b;
+  p.c = c;
+  p.eps = eps;
+  p.gram_mode = gram_mode;
+  p.ridge = ridge;
+  rc = nsplan::build_two_stage(p, n_tensors, ndims, shapes_flat, partition_dims, R, T, home_of);
   if (rc != NS_OK) {
     delete pl;
     return rc;

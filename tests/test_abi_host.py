@@ -214,3 +214,28 @@ def test_workspace_bytes_layout():
     assert lower <= ws <= lower + 64 * 1024
     assert plan.n_buckets == 2
     assert nsg.ns_plan_create([], S=1).workspace_bytes() == 0
+
+
+@pytest.mark.parametrize("R,T", [(1, 1), (2, 2), (4, 2), (2, 4)])
+def test_two_stage_plan_vs_oracle(R, T):
+    shapes = [(32, 16), (16, 32, 2), (64, 8), (8, 8, 8), (16, 24)]
+    pd = [1, 1, 0, 2, 1]
+    plan = nsg.ns_plan_create_two_stage(shapes, pd, R, T)
+    S = R * T
+    want = op.lpt_homes_row_shard(shapes, S)
+    assert plan.homes() == [want[i] for i in range(len(shapes))]
+    ho, hs, rs = plan.home_layout()
+    assert ho == orr.home_offsets(shapes, want, S)
+    assert rs == [sum(int(np.prod(s)) // S for s in shapes)] * S
+
+
+def test_two_stage_errors():
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_plan_create_two_stage([(6, 8)], [0], 2, 2)   # 6 rows not divisible by R*T = 4
+    assert e.value.code == nsg.NS_ERR_NOT_DIVISIBLE
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_plan_create_two_stage([(8, 6)], [1], 2, 4)   # 6 columns not divisible by T = 4
+    assert e.value.code == nsg.NS_ERR_NOT_DIVISIBLE
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_plan_create_two_stage([(8, 8)], [2], 2, 2)   # no dim 2
+    assert e.value.code == nsg.NS_ERR_ARG

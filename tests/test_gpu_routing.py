@@ -107,3 +107,32 @@ def test_flat_random(S):
         pos += int(np.prod(shp))
     size = ((pos + S - 1) // S) * S
     _flat_case(shapes, offsets, size, S, 40 + S)
+
+
+@pytest.mark.parametrize("R,T", [(2, 2), (2, 4), (4, 2), (1, 4), (3, 1)])
+def test_two_stage_fused_gather_equals_two_stages(R, T):
+    # one fused gather on the GPU == GTP_remat stage (dim 0) then TP stage
+    # (partition_dim), done literally by the oracle
+    shapes = [(48, 24), (24, 48, 4), (96, 16), (24, 8, 8), (48, 12)]
+    pd = [1, 1, 0, 2, 1]
+    dev = torch.device("cuda:0")
+    ts = workloads.gen_tensors(workloads.Workload("two", shapes, 1.0, 91))
+    np_ts = [bits(t).reshape(t.shape) for t in ts]
+    plan = nsg.ns_plan_create_two_stage(shapes, pd, R, T)
+    S = R * T
+    home_of = dict(enumerate(plan.homes()))
+    ranks = orr.make_rank_buffers_two_stage(np_ts, R, T, pd)
+    want = orr.route_two_stage(ranks, shapes, pd, home_of, R, T)
+    rank_t = [torch.from_numpy(r.view(np.int16).copy()).view(torch.bfloat16).to(dev) for r in ranks]
+    _, hs, _ = plan.home_layout()
+    home_t = [torch.full((max(1, n),), -3.0, dtype=torch.bfloat16, device=dev) for n in hs]
+    nsg.ns_pack_to_home(plan, rank_t, home_t)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for h in range(S):
+        assert np.array_equal(bits(home_t[h])[:hs[h]], want[h])
+    back = [torch.zeros_like(r) for r in rank_t]
+    nsg.ns_unpack_from_home(plan, home_t, back)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    back_want = orr.route_two_stage_back(want, shapes, pd, home_of, R, T)
+    for r in range(S):
+        assert np.array_equal(bits(back[r]), back_want[r])
