@@ -40,7 +40,7 @@ UNIT = "matrices/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe", "sweep"], default="gpt")
@@ -164,7 +164,7 @@ class ClockSampler:
 
     def start(self):
         try:
-            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
             if self.gpu_id:
                 cmd += ["-i", self.gpu_id]
             self.f = open(self.path, "w")

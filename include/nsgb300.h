@@ -50,7 +50,12 @@ enum {
 /* Precision policy of a plan (gram_mode). */
 enum {
   NS_BF16 = 0,      /* bf16 X, A, B operands, fp32 accumulation and epilogues; bf16 in, bf16 out */
-  NS_FP32_GRAM = 1  /* fp32 X, A, B: TF32 Gram, split-TF32 A*A and B*X; bf16 in, fp32 out */
+  NS_FP32_GRAM = 1, /* fp32 X, A, B as split-TF32 (hi, lo) pairs; bf16 in, fp32 out */
+  /* [ISS] Gram-space NS ("gram_once"), same fp32 precision: A = X X^T once, then
+   * per step Q = aI + bA + cA^2, A <- Q A Q, P <- Q P on m x m matrices only,
+   * and X_k = P X_0 at the end. Exact reformulation of the same iteration;
+   * fewer flops when n is well above m. bf16 in, fp32 out. */
+  NS_FP32_GRAM_SPACE = 2
 };
 
 /* Data model of a plan. */

@@ -218,16 +218,32 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm32_kernel(const __grid_cons
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
         if (PHASE == PH32_A2B) {
-          // B = b*A + c*(A A); A = hi + lo
-          const float4* h4 = reinterpret_cast<const float4*>(B.aux_h + mo + static_cast<long long>(r) * B.ld + cg);
-          const float4* l4 = reinterpret_cast<const float4*>(B.aux_l + mo + static_cast<long long>(r) * B.ld + cg);
+          // out = delta*I + beta*aux + gamma*(L R); aux = hi + lo (standard
+          // step: B = b*A + c*(A A); Gram-space steps: Q, Q*A, Q*T, Q*P)
+          float dl = B.delta, be = B.beta, ga = B.gamma;
+          if (B.coef) {
+            dl = B.coef[3 * mat];
+            be = B.coef[3 * mat + 1];
+            ga = B.coef[3 * mat + 2];
+          }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 h = h4[q], l = l4[q];
-            f[4 * q + 0] = p.beta * (h.x + l.x) + p.gamma * f[4 * q + 0];
-            f[4 * q + 1] = p.beta * (h.y + l.y) + p.gamma * f[4 * q + 1];
-            f[4 * q + 2] = p.beta * (h.z + l.z) + p.gamma * f[4 * q + 2];
-            f[4 * q + 3] = p.beta * (h.w + l.w) + p.gamma * f[4 * q + 3];
+          for (int j = 0; j < 32; ++j) f[j] *= ga;
+          if (B.aux_h) {
+            const float4* h4 = reinterpret_cast<const float4*>(B.aux_h + mo + static_cast<long long>(r) * B.ld + cg);
+            const float4* l4 = reinterpret_cast<const float4*>(B.aux_l + mo + static_cast<long long>(r) * B.ld + cg);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 h = h4[q], l = l4[q];
+              f[4 * q + 0] += be * (h.x + l.x);
+              f[4 * q + 1] += be * (h.y + l.y);
+              f[4 * q + 2] += be * (h.z + l.z);
+              f[4 * q + 3] += be * (h.w + l.w);
+            }
+          }
+          if (r >= cg && r < cg + 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (cg + j == r) f[j] += dl;
           }
         }
         if (SYRK) {
@@ -336,8 +352,9 @@ cudaError_t launch32(const P& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Trace ridge: A <- A + ridge * (trace(A) / m) * I on the (hi, lo) pair.
-// One CTA per matrix; fixed-order reduction.
+// Trace ridge r = ridge * trace(A) / m, one CTA per matrix (fixed-order
+// reduction). Standard step: A <- A + r I on the (hi, lo) pair. Gram-space
+// step (coef set): write that matrix's Q coefficients instead.
 __global__ void __launch_bounds__(256) ns_ridge32_kernel(const __grid_constant__ Ridge32Params p) {
   const Ridge32Bucket& B = p.bk[blockIdx.y];
   if (static_cast<int>(blockIdx.x) >= B.count) return;
@@ -355,7 +372,19 @@ __global__ void __launch_bounds__(256) ns_ridge32_kernel(const __grid_constant__
     if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
     __syncthreads();
   }
-  const float delta = static_cast<float>(static_cast<double>(p.ridge) * red[0] / B.m);
+  const double rr = static_cast<double>(p.ridge) * red[0] / B.m;
+  if (p.coef[blockIdx.y]) {
+    // Gram-space step: Q = aI + b(A + rI) + c(A + rI)^2
+    //                    = (a + b r + c r^2) I + (b + 2 c r) A + c A^2
+    if (threadIdx.x == 0) {
+      float* cf = p.coef[blockIdx.y] + 3 * blockIdx.x;
+      cf[0] = static_cast<float>(p.a + p.b * rr + p.c * rr * rr);
+      cf[1] = static_cast<float>(p.b + 2.0 * p.c * rr);
+      cf[2] = p.c;
+    }
+    return;
+  }
+  const float delta = static_cast<float>(rr);
   __syncthreads();
   for (int i = threadIdx.x; i < B.m; i += blockDim.x) {
     const long long d = static_cast<long long>(i) * B.ld + i;

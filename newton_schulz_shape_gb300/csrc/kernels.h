@@ -63,8 +63,10 @@ struct Gemm32Bucket {
   float* out_l;
   float* out_th;           // BXT: next X^T hi (n_pad x m_pad)
   float* out_tl;
-  const float* aux_h;      // A2B: A hi; BXT: current X hi
+  const float* aux_h;      // A2B: A hi (may be null: no aux term); BXT: current X hi
   const float* aux_l;
+  const float* coef;       // A2B: per-matrix (delta, beta, gamma) or null (use delta/beta/gamma below)
+  float delta, beta, gamma;  // A2B: out = delta*I + beta*aux + gamma*acc when coef is null
   int count, tiles_m, tiles_n, tiles_per_mat, k_blocks;
   int ld;                  // leading dimension of out_h/out_l/aux (elements)
   int ld_t;                // leading dimension of out_th/out_tl
@@ -103,6 +105,8 @@ struct Ridge32Params {
   Ridge32Bucket bk[GEMM_MAX_BUCKETS];
   int nb, max_count;
   float ridge;
+  float a, b, c;          // Gram-space coefficients: writes coef = (a + b r + c r^2, b + 2 c r, c)
+  float* coef[GEMM_MAX_BUCKETS];  // null: add the ridge to A's diagonal instead
 };
 
 // ------------------------------------------------------- prologue / store

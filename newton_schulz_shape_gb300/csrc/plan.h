@@ -40,6 +40,7 @@ struct Bucket {
   uint64_t off_x0 = 0, off_x1 = 0, off_a = 0, off_b = 0;  // workspace byte offsets
   uint64_t off_partial = 0;  // float partial sums: count * nchunks
   uint64_t off_scale = 0;    // float scale per member
+  uint64_t off_coef = 0;     // fp32 Gram-space: 3 floats per member (Q coefficients)
   int64_t nchunks = 0;       // sum-of-squares chunks per matrix
 };
 

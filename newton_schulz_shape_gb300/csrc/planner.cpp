@@ -95,7 +95,7 @@ int finish(Plan& p) {
       b.n = t.n;
       b.m_pad = round_up(t.m, nsk::GEMM_BM);
       // fp32-Gram: n is also the M dimension of the (B X)^T product, tiled by 128
-      b.n_pad = round_up(t.n, p.gram_mode == NS_FP32_GRAM ? nsk::GEMM_BM : nsk::GEMM_BK);
+      b.n_pad = round_up(t.n, p.gram_mode != NS_BF16 ? nsk::GEMM_BM : nsk::GEMM_BK);
       index[key] = static_cast<int>(p.buckets.size());
       p.buckets.push_back(b);
       it = index.find(key);
@@ -111,7 +111,10 @@ int finish(Plan& p) {
   // bf16 path: one bf16 copy of X per ping-pong buffer, A and B in bf16.
   // fp32-Gram path: X as (hi, lo) fp32 pairs, both m-major and transposed
   // (4 buffers per ping-pong set); A and B as (hi, lo) fp32 pairs.
-  const bool f32 = p.gram_mode == NS_FP32_GRAM;
+  // fp32 Gram-space path: one X set, then (hi, lo) pairs of T, P0, P1 in the
+  // second X region.
+  const bool f32 = p.gram_mode != NS_BF16;
+  const bool gs = p.gram_mode == NS_FP32_GRAM_SPACE;
   const uint64_t xset = f32 ? 4 * 4 : 2;
   const uint64_t aset = f32 ? 2 * 4 : 2;
   uint64_t off = 0;
@@ -131,12 +134,13 @@ int finish(Plan& p) {
     const uint64_t xbytes = cnt * uint64_t(b.m_pad) * uint64_t(b.n_pad) * xset;
     const uint64_t abytes = cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * aset;
     b.off_x0 = take(xbytes);
-    b.off_x1 = take(xbytes);
+    b.off_x1 = take(gs ? cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * 3 * aset : xbytes);
     b.off_a = take(abytes);
     b.off_b = take(abytes);
     b.nchunks = (b.m * b.n + kSumsqChunk - 1) / kSumsqChunk;
     b.off_partial = take(cnt * uint64_t(b.nchunks) * 4);
     b.off_scale = take(cnt * 4);
+    b.off_coef = take(cnt * 3 * 4);
   }
   p.ws_bytes = p.buckets.empty() ? 0 : (off + 1023) / 1024 * 1024;
   // routing table: one entry per participating tensor with data on the ranks
@@ -164,7 +168,7 @@ int finish(Plan& p) {
     p.route.push_back(e);
   }
   p.in_bytes = 2;
-  p.out_bytes = p.gram_mode == NS_FP32_GRAM ? 4 : 2;
+  p.out_bytes = p.gram_mode != NS_BF16 ? 4 : 2;
   return NS_OK;
 }
 
@@ -441,7 +445,7 @@ namespace {
 int check_coeffs(int steps, float eps, int gram_mode, float ridge) {
   if (steps < 0) return NS_ERR_ARG;
   if (!(eps >= 0.0f)) return NS_ERR_ARG;
-  if (gram_mode != NS_BF16 && gram_mode != NS_FP32_GRAM) return NS_ERR_ARG;
+  if (gram_mode != NS_BF16 && gram_mode != NS_FP32_GRAM && gram_mode != NS_FP32_GRAM_SPACE) return NS_ERR_ARG;
   if (!(ridge >= 0.0f)) return NS_ERR_ARG;
   if (gram_mode == NS_BF16 && ridge != 0.0f) return NS_ERR_ARG;
   return NS_OK;

@@ -94,3 +94,57 @@ def test_fp32_gram_beats_bf16_path():
     nsg.ns_orthogonalize_batched(plan, [x], [y], ws)
     bf16 = rel_err(y, ref)
     assert f32 < bf16 / 10, (f32, bf16)
+
+
+def run_mode(shapes, ts, mode, steps=workloads.STEPS, ridge=0.0):
+    dev = torch.device("cuda:0")
+    ins = [t.to(dev) for t in ts]
+    outs = [torch.full(t.shape, float("nan"), dtype=torch.float32, device=dev) for t in ins]
+    plan = nsg.ns_plan_create(shapes, steps=steps, eps=workloads.EPS, gram_mode=mode, ridge=ridge, S=1)
+    ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    rc = nsg.ns_check_status(plan)
+    assert rc == nsg.NS_OK, nsg.ns_status_string(rc)
+    return outs
+
+
+# Gram-space NS (issue #6720's gram_once): the same iteration carried on m x m
+# matrices; the result must match the oracle of the standard iteration.
+GS_SHAPES = [(128, 512), (512, 128), (256, 64, 3, 3), (200, 900), (130, 130), (5, 3)]
+
+
+def test_gram_space_matches_oracle():
+    ts = workloads.gen_tensors(workloads.Workload("gs", GS_SHAPES, 1.0, 81))
+    outs = run_mode(GS_SHAPES, ts, nsg.NS_FP32_GRAM_SPACE)
+    for s, t, o in zip(GS_SHAPES, ts, outs):
+        assert o.shape == t.shape
+        err = rel_err(o, oracle(t))
+        assert err <= FP32_TOL, (s, err)
+
+
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_gram_space_step_counts(steps):
+    shapes = [(256, 1024), (1024, 256)]
+    ts = workloads.gen_tensors(workloads.Workload("gss", shapes, 0.02, 82))
+    outs = run_mode(shapes, ts, nsg.NS_FP32_GRAM_SPACE, steps=steps)
+    for t, o in zip(ts, outs):
+        assert rel_err(o, oracle(t, steps)) <= FP32_TOL
+
+
+@pytest.mark.parametrize("ridge", [1e-5, 1e-3])
+def test_gram_space_trace_ridge(ridge):
+    shapes = [(256, 1024), (300, 800)]
+    ts = workloads.gen_tensors(workloads.Workload("gsr", shapes, 0.02, 83))
+    outs = run_mode(shapes, ts, nsg.NS_FP32_GRAM_SPACE, ridge=ridge)
+    for t, o in zip(ts, outs):
+        assert rel_err(o, oracle(t, ridge=ridge)) <= FP32_TOL
+
+
+def test_gram_space_agrees_with_fp32_gram_path():
+    shapes = [(1024, 4096), (2048, 2048)]
+    ts = workloads.gen_tensors(workloads.Workload("gsa", shapes, 0.02, 84))
+    a = run_mode(shapes, ts, nsg.NS_FP32_GRAM_SPACE)
+    b = run_mode(shapes, ts, nsg.NS_FP32_GRAM)
+    for t, x, y in zip(ts, a, b):
+        assert rel_err(x, y.cpu().numpy()) <= FP32_TOL
+        assert rel_err(x, oracle(t)) <= FP32_TOL
