@@ -44,8 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe", "sweep"], default="gpt")
-    ap.add_argument("--gram", choices=["bf16", "fp32"], default="bf16",
-                    help="precision policy (sweep workload): bf16 path or fp32-Gram (split TF32) path")
+    ap.add_argument("--gram", choices=["bf16", "fp32", "fp32gs"], default="bf16",
+                    help="precision policy (sweep workload): bf16 path, fp32-Gram (split TF32) path, "
+                         "or its Gram-space form")
     ap.add_argument("--ridge", type=float, default=0.0, help="trace ridge (fp32-Gram path only)")
     ap.add_argument("--points", type=str, default="",
                     help="sweep subset, e.g. '1024x1,4096x8' (m x aspect); default: all")
@@ -112,17 +113,28 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def traffic_for(kernel: str):
+def gemm_kernel_for(kind: str, cluster_mode: int):
+    """(kernel name, source file) of the GEMM kind under a tiling mode: the
+    library's default runs the 2-SM kernel for Gram and B*X, the 1-SM kernel
+    for A*A."""
+    mode = cluster_mode if cluster_mode else (1 if kind == "a2b" else 3)
+    if mode == 3:
+        return f"ns_gemm2sm_kernel<{kind}>", "gemm2sm.cu"
+    return f"ns_gemm_kernel<{kind}>", "gemm.cu"
+
+
+def traffic_for(kind: str, cluster_mode: int):
     """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    src = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc", "gemm.cu")
+    on the current source of that kernel (else None)."""
+    name, fname = gemm_kernel_for(kind, cluster_mode)
+    src = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc", fname)
     summ = os.path.join(ROOT, "profiles", "gemm_traffic.md")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         for line in open(summ):
             if line.startswith("traffic:"):
                 kv = dict(x.strip().split("=", 1) for x in line[len("traffic:"):].split(";") if "=" in x)
-                if kv.get("kernel") == kernel and kv.get("gemm_cu_sha256") == sha:
+                if kv.get("kernel") == name and kv.get("source") == fname and kv.get("sha256") == sha:
                     return int(kv["dram_bytes_per_launch"])
     except Exception:
         return None
@@ -469,8 +481,9 @@ def run_ours(args):
     flops_per_launch = fl[dom] / launches_per_step
     achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
     useful = sum(fl.values())
-    roofline = {"bound": "tensor", "kernel": f"ns_gemm_kernel<{dom}>", "achieved": achieved, "peak": sustained,
-                "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": traffic_for(dom),
+    roofline = {"bound": "tensor", "kernel": gemm_kernel_for(dom, args.gemm_cluster)[0], "achieved": achieved,
+                "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
+                "traffic": traffic_for(dom, args.gemm_cluster),
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); burst {burst}",
                 "flops_per_launch": flops_per_launch, "avg_launch_ms": per_launch_ms}
     per_kernel = {k: {"launches_per_step": launches[k] / args.steps, "ms_per_step": kms[k] / args.steps}
@@ -525,7 +538,7 @@ def run_sweep(args):
     if args.points:
         want = {tuple(int(x) for x in p.split("x")) for p in args.points.split(",")}
         pts = [p for p in pts if (p[0], p[1]) in want]
-    mode = nsg.NS_FP32_GRAM if args.gram == "fp32" else nsg.NS_BF16
+    mode = {"bf16": nsg.NS_BF16, "fp32": nsg.NS_FP32_GRAM, "fp32gs": nsg.NS_FP32_GRAM_SPACE}[args.gram]
     stream = torch.cuda.current_stream(dev)
     results, tot_ms, tot_mats, tot_flops = [], 0.0, 0, 0
     runs = [(f"{m}x{a * m}", [(m, a * m)] * bt, 5000 + m + a) for (m, a, bt) in pts]
@@ -536,7 +549,7 @@ def run_sweep(args):
     for name, shapes, seed in runs:
         w = workloads.Workload(name, shapes, 0.02, seed)
         ins = [workloads.gen_tensor(s, w.sigma, w.seed, i).to(dev) for i, s in enumerate(shapes)]
-        odt = torch.float32 if mode == nsg.NS_FP32_GRAM else torch.bfloat16
+        odt = torch.bfloat16 if mode == nsg.NS_BF16 else torch.float32
         outs = [torch.empty(s, dtype=odt, device=dev) for s in shapes]
         plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, gram_mode=mode,
                                   ridge=args.ridge, S=1)
