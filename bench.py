@@ -54,6 +54,8 @@ def parse():
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2, 3],
                     help="GEMM tiling: 0 automatic, 1 single CTA, 2 multicast CTA pairs, 3 2-SM MMA")
+    ap.add_argument("--waves", type=int, default=0,
+                    help="run the step through the wave pipeline with this many waves (0: serial calls)")
     ap.add_argument("--split-qkv", action="store_true",
                     help="orthogonalise Q, K and V blocks of fused QKV projections separately")
     ap.add_argument("--no-e2e", action="store_true")
@@ -342,10 +344,22 @@ def run_ours(args):
         ws = torch.empty(ns_plan.workspace_bytes(), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
+    pipe = None
+    if args.waves > 0:
+        if args.split_qkv:
+            raise SystemExit("--waves and --split-qkv do not combine")
+        pipe = nsg.ns_pipeline_create(plan, args.waves)
+        ws = torch.empty(pipe.workspace_bytes, dtype=torch.uint8, device=dev)
+
+    def step(rin=None, rout=None):
+        rin = rank_in if rin is None else rin
+        rout = rank_out if rout is None else rout
+        if pipe is not None:
+            nsg.ns_pipeline_run(pipe, rin, home_in, home_out, rout, ws, stream=stream)
+            return
+        nsg.ns_pack_to_home(plan, rin, home_in, stream=stream)
         nsg.ns_orthogonalize_batched(ns_plan, ins, outs, ws, stream=stream)
-        nsg.ns_unpack_from_home(plan, home_out, rank_out, stream=stream)
+        nsg.ns_unpack_from_home(plan, home_out, rout, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -376,6 +390,13 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
+        if pipe is not None:
+            # the pipeline overlaps the phases; only whole steps are timed
+            ev[k][0].record(stream)
+            step()
+            for j in (1, 2, 3):
+                ev[k][j].record(stream)
+            continue
         ev[k][0].record(stream)
         nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
         ev[k][1].record(stream)
@@ -440,9 +461,7 @@ def run_ours(args):
                 stream.wait_event(ev_in[b])
                 if k >= 2:
                     stream.wait_event(ev_out[b])       # rank_out[b] was copied out by step k-2
-                nsg.ns_pack_to_home(plan, rin[b], home_in, stream=stream)
-                nsg.ns_orthogonalize_batched(ns_plan, ins, outs, ws, stream=stream)
-                nsg.ns_unpack_from_home(plan, home_out, rout[b], stream=stream)
+                step(rin[b], rout[b])
                 ev_cmp[b].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_cmp[b])
@@ -500,13 +519,15 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
                                f"pack -> NS (5 steps) -> unpack",
                    "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS, "gemm_cluster": args.gemm_cluster,
-                   "split_qkv": bool(args.split_qkv),
+                   "split_qkv": bool(args.split_qkv), "waves": args.waves,
                    "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
         "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
-        "ns_only": {"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,
-                    "frac_of_burst_peak": useful / (ns_ms * 1e-3) / 1e12 / burst},
-        "phases_ms": {"pack": pack_ms, "ns": ns_ms, "unpack": unpack_ms},
-        "pack_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9, "unpack_gbs": pack_bytes / (unpack_ms * 1e-3) / 1e9,
+        "ns_only": ({"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,
+                     "frac_of_burst_peak": useful / (ns_ms * 1e-3) / 1e12 / burst} if pipe is None else None),
+        "phases_ms": ({"pack": pack_ms, "ns": ns_ms, "unpack": unpack_ms} if pipe is None
+                      else {"pipelined_step": pack_ms, "waves": pipe.n_waves}),
+        "pack_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9 if pipe is None else None,
+        "unpack_gbs": pack_bytes / (unpack_ms * 1e-3) / 1e9 if pipe is None and unpack_ms > 0 else None,
         "per_kernel": per_kernel,
         "clocks": clk,
         "e2e": e2e,

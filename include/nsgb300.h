@@ -209,6 +209,29 @@ int ns_pack_to_home(ns_plan_t* plan, const void* const* rank_bufs, int S, int sh
 int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, int shard_dim,
                         void* const* rank_bufs, void* stream);
 
+/* [ISS] wave dispatch, single-GPU form. A pipeline splits the plan's
+ * participating tensors (bf16 plans only, else NS_ERR_UNSUPPORTED) into at
+ * most n_waves waves of consecutive tensors with balanced ns_cost. The plan
+ * must outlive the pipeline. ns_pipeline_run then performs pack ->
+ * Newton-Schulz -> unpack for the whole plan, with the same results as
+ * ns_pack_to_home + ns_orthogonalize_batched + ns_unpack_from_home. Work runs
+ * on three streams owned by the pipeline: the pack and prologue of a wave
+ * overlap the NS products of the previous wave, and the unpack of a wave
+ * overlaps the next one. Buffers as in ns_pack_to_home / ns_unpack_from_home
+ * (home_in receives the gathered inputs, home_out the results). workspace
+ * holds two wave workspaces (ns_pipeline_info), 256-byte aligned. The call
+ * is ordered after prior work on `stream`, and later work on `stream` waits
+ * for all of it. The first run on a device creates the pipeline's streams
+ * and events: make it before any stream capture. Runs that overlap on the
+ * GPU must not share a pipeline or a workspace. */
+typedef struct ns_pipeline ns_pipeline_t;
+int ns_pipeline_create(ns_plan_t* plan, int n_waves, ns_pipeline_t** pipeline_out);
+int ns_pipeline_info(const ns_pipeline_t* pipeline, int* n_waves, uint64_t* workspace_bytes);
+int ns_pipeline_run(ns_pipeline_t* pipeline, const void* const* rank_in, void* const* home_in,
+                    void* const* home_out, void* const* rank_out, void* workspace, uint64_t workspace_bytes,
+                    void* stream);
+int ns_pipeline_destroy(ns_pipeline_t* pipeline);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: NS_ERR_TIMEOUT or NS_ERR_DEVICE_CHECK if a kernel recorded one, else
  * NS_ERR_CUDA on a pending CUDA error, else NS_OK. plan may be NULL. */

@@ -251,3 +251,36 @@ def ns_set_gemm_cluster(cl: int) -> None:
     """GEMM tiling: 0 automatic (2-SM MMA for Gram and B*X, single CTA for A*A),
     1 single CTA, 2 multicast pairs, 3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")
+
+
+class NsPipeline:
+    """Owns an ns_pipeline_t* (wave-dispatched pack -> NS -> unpack)."""
+
+    def __init__(self, plan: NsPlan, n_waves: int):
+        self.plan = plan          # keeps the plan alive
+        self._h = ctypes.c_void_p()
+        check(lib.ns_pipeline_create(plan.handle, n_waves, ctypes.byref(self._h)), "ns_pipeline_create")
+        w = ctypes.c_int()
+        b = ctypes.c_uint64()
+        check(lib.ns_pipeline_info(self._h, ctypes.byref(w), ctypes.byref(b)), "ns_pipeline_info")
+        self.n_waves = w.value
+        self.workspace_bytes = b.value
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.ns_pipeline_destroy(h)
+            self._h = None
+
+
+def ns_pipeline_create(plan: NsPlan, n_waves: int) -> NsPipeline:
+    return NsPipeline(plan, n_waves)
+
+
+def ns_pipeline_run(pipe: NsPipeline, rank_in, home_in, home_out, rank_out, workspace, stream=None) -> None:
+    """Wave-dispatched pack -> Newton-Schulz -> unpack over the whole plan."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib.ns_pipeline_run(pipe._h, ptr_array([_addr(t) for t in rank_in]),
+                              ptr_array([_addr(t) for t in home_in]), ptr_array([_addr(t) for t in home_out]),
+                              ptr_array([_addr(t) for t in rank_out]), _addr(workspace), nbytes, _stream(stream)),
+          "ns_pipeline_run")

@@ -67,6 +67,11 @@ _SIGS = {
     "ns_unpack_from_home": (ctypes.c_int, [_planp, _vpp, ctypes.c_int, ctypes.c_int, _vpp, ctypes.c_void_p]),
     "ns_check_status": (ctypes.c_int, [_planp, ctypes.c_void_p]),
     "ns_orthogonalize_batched_fixed_ws": (ctypes.c_int, [_planp, _vpp, _vpp, ctypes.c_int, ctypes.c_void_p]),
+    "ns_pipeline_create": (ctypes.c_int, [_planp, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)]),
+    "ns_pipeline_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), _u64p]),
+    "ns_pipeline_run": (ctypes.c_int, [ctypes.c_void_p, _vpp, _vpp, _vpp, _vpp, ctypes.c_void_p, ctypes.c_uint64,
+                                       ctypes.c_void_p]),
+    "ns_pipeline_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "ns_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "ns_set_gemm_cluster": (ctypes.c_int, [ctypes.c_int]),
     "ns_profile_read": (ctypes.c_int, [ctypes.c_int, _i64p, ctypes.POINTER(ctypes.c_double)]),

@@ -159,6 +159,8 @@ struct PackParams {
   long long n_entries;
   long long rank_len;   // positions per rank buffer
   long long chunk;      // positions per CTA
+  long long g_begin;    // entry-coordinate range to move (a wave of the pipeline, or everything)
+  long long g_end;
   int S;
   int T;                // TP ranks of the two-stage model (1 otherwise)
   int flat;             // 1: flat-buffer model, 0: row-shard / two-stage model

@@ -22,6 +22,7 @@
 // search, then copies every contiguous run it overlaps with 16-byte vectors
 // (falling back to 4- or 2-byte words where source and destination
 // alignments differ). Bit-exact.
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -77,11 +78,14 @@ __device__ __forceinline__ void copy_run(char* dst, const char* src, long long b
 
 __global__ void __launch_bounds__(PACK_THREADS) ns_pack_kernel(const __grid_constant__ PackParams p) {
   const int r = blockIdx.y;
-  const long long p0 = static_cast<long long>(blockIdx.x) * p.chunk;
-  if (p0 >= p.rank_len) return;
-  const long long p1 = min(p.rank_len, p0 + p.chunk);
-  // entry coordinates: per-rank positions (row-shard) or global positions (flat)
+  // entry coordinates: per-rank positions (row-shard, two-stage) or global
+  // positions (flat); this rank's share of [g_begin, g_end) in its own buffer
   const long long base = p.flat ? static_cast<long long>(r) * p.rank_len : 0;
+  const long long lo_local = max(0ll, p.g_begin - base);
+  const long long hi_local = min(p.rank_len, p.g_end - base);
+  const long long p0 = lo_local + static_cast<long long>(blockIdx.x) * p.chunk;
+  if (p0 >= hi_local) return;
+  const long long p1 = min(hi_local, p0 + p.chunk);
   const long long g0 = base + p0, g1 = base + p1;
   // first entry whose end is past g0
   long long lo = 0, hi = p.n_entries;
@@ -131,8 +135,9 @@ __global__ void __launch_bounds__(PACK_THREADS) ns_pack_kernel(const __grid_cons
 }  // namespace
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t st) {
-  if (p.rank_len <= 0 || p.n_entries <= 0 || p.S <= 0) return cudaSuccess;
-  const long long nchunks = (p.rank_len + p.chunk - 1) / p.chunk;
+  if (p.rank_len <= 0 || p.n_entries <= 0 || p.S <= 0 || p.g_end <= p.g_begin) return cudaSuccess;
+  const long long span = std::min(p.rank_len, p.g_end - p.g_begin);  // positions per rank at most
+  const long long nchunks = (span + p.chunk - 1) / p.chunk + (p.flat ? 1 : 0);
   ns_pack_kernel<<<dim3(static_cast<unsigned>(nchunks), p.S), PACK_THREADS, 0, st>>>(p);
   return cudaGetLastError();
 }

@@ -72,6 +72,7 @@ int build_flat(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, cons
                int64_t size, const uint8_t* participating, int S, const int32_t* owner_of);
 int lpt_assign(int n, const int64_t* costs, const int32_t* cand_ptr, const int32_t* cand_idx, int n_ranks,
                int32_t* owner_out);
+int build_subplan(const Plan& base, const std::vector<int>& members, Plan& out);
 
 }  // namespace nsplan
 

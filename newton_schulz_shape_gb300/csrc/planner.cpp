@@ -69,19 +69,24 @@ int load_tensors(Plan& p, int n, const int32_t* ndims, const int64_t* shapes, bo
   return NS_OK;
 }
 
-// Home buffers, buckets, workspace layout and routing table.
-int finish(Plan& p) {
+// Home buffers, buckets, workspace layout and routing table. keep_homes: a
+// sub-plan of a pipeline wave keeps the whole plan's home offsets and sizes.
+int finish(Plan& p, bool keep_homes = false) {
   // participating list and home offsets (increasing index order per home)
   p.part.clear();
-  p.home_sizes.assign(p.S, 0);
+  if (!keep_homes) p.home_sizes.assign(p.S, 0);
   for (size_t i = 0; i < p.t.size(); ++i) {
     Tensor& t = p.t[i];
+    t.bucket = t.slot = -1;
     if (!t.participating) continue;
     t.ordinal = static_cast<int>(p.part.size());
     p.part.push_back(static_cast<int>(i));
-    t.home_off = p.home_sizes[t.home];
-    p.home_sizes[t.home] += t.numel;
+    if (!keep_homes) {
+      t.home_off = p.home_sizes[t.home];
+      p.home_sizes[t.home] += t.numel;
+    }
   }
+  p.buckets.clear();
   // buckets of equal (m, n), heaviest per-matrix work first
   std::map<std::pair<int64_t, int64_t>, int> index;
   for (int i : p.part) {
@@ -173,6 +178,18 @@ int finish(Plan& p) {
 }
 
 }  // namespace
+
+// NS-only sub-plan over `members` (tensor indices, increasing) of `base`:
+// same tensors, homes and home offsets; buckets and workspace of the members.
+int build_subplan(const Plan& base, const std::vector<int>& members, Plan& out) {
+  out = base;
+  for (Tensor& t : out.t) t.participating = false;
+  for (int i : members) out.t[i].participating = true;
+  for (void*& d : out.d_route) d = nullptr;  // device tables stay with the base plan
+  int rc = finish(out, true);
+  out.route.clear();
+  return rc;
+}
 
 int lpt_assign(int n, const int64_t* costs, const int32_t* cand_ptr, const int32_t* cand_idx, int n_ranks,
                int32_t* owner_out) {

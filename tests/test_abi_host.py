@@ -239,3 +239,18 @@ def test_two_stage_errors():
     with pytest.raises(nsg.NsError) as e:
         nsg.ns_plan_create_two_stage([(8, 8)], [2], 2, 2)   # no dim 2
     assert e.value.code == nsg.NS_ERR_ARG
+
+
+def test_pipeline_wave_split_host():
+    w = workloads.gpt_24l_d2048()
+    plan = nsg.ns_plan_create(w.shapes, S=8)
+    for n in (1, 2, 4, 7, 500):
+        pipe = nsg.ns_pipeline_create(plan, n)
+        assert 1 <= pipe.n_waves <= min(n, len(w.shapes))
+        assert pipe.workspace_bytes > 0
+        # two wave workspaces, each at most the whole plan's
+        assert pipe.workspace_bytes <= 2 * plan.workspace_bytes() + 2048
+    fp32 = nsg.ns_plan_create([(128, 256)], gram_mode=nsg.NS_FP32_GRAM, S=1)
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_pipeline_create(fp32, 2)
+    assert e.value.code == nsg.NS_ERR_UNSUPPORTED

@@ -136,3 +136,46 @@ def test_two_stage_fused_gather_equals_two_stages(R, T):
     back_want = orr.route_two_stage_back(want, shapes, pd, home_of, R, T)
     for r in range(S):
         assert np.array_equal(bits(back[r]), back_want[r])
+
+
+@pytest.mark.parametrize("n_waves", [1, 2, 3, 7])
+def test_wave_pipeline_equals_serial_step(n_waves):
+    # issue #6720 wave dispatch: the pipelined pack -> NS -> unpack must give
+    # the serial result bit for bit
+    w = workloads.gpt_24l_d2048()
+    w.shapes = w.shapes[:8] + [(640, 384), (384, 640), (256, 64, 3, 3)]
+    S, shapes = w.S, w.shapes
+    dev = torch.device("cuda:0")
+    ts = workloads.gen_tensors(w)
+    plan = nsg.ns_plan_create(shapes, S=S, shard_dim=0)
+    homes = plan.homes()
+    ho, hs, rs = plan.home_layout()
+    rank_in = [torch.cat([t.reshape(S, -1)[r] for t in ts]).to(dev) for r in range(S)]
+
+    def bufs():
+        return ([torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs],
+                [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs],
+                [torch.zeros_like(x) for x in rank_in])
+
+    hi1, ho1, ro1 = bufs()
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ins = [hi1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))]
+    outs = [ho1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))]
+    nsg.ns_pack_to_home(plan, rank_in, hi1)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    nsg.ns_unpack_from_home(plan, ho1, ro1)
+    hi2, ho2, ro2 = bufs()
+    pipe = nsg.ns_pipeline_create(plan, n_waves)
+    pws = torch.empty(pipe.workspace_bytes, dtype=torch.uint8, device=dev)
+    for _ in range(2):   # run twice: the second run reuses streams, events and workspaces
+        nsg.ns_pipeline_run(pipe, rank_in, hi2, ho2, ro2, pws)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for a, b in zip(ho1, ho2):
+        assert torch.equal(a, b)
+    for a, b in zip(ro1, ro2):
+        assert torch.equal(a, b)
+    # and the serial result itself is right (sampled)
+    for i in (0, 3, len(shapes) - 1):
+        y = ho2[homes[i]][ho[i]:ho[i] + ts[i].numel()].reshape(ts[i].shape)
+        from gpu_util import BF16_TOL, oracle_ns, rel_err
+        assert rel_err(y, oracle_ns(ts[i])) <= BF16_TOL
