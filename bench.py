@@ -54,7 +54,7 @@ def parse():
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2, 3],
                     help="GEMM tiling: 0 automatic, 1 single CTA, 2 multicast CTA pairs, 3 2-SM MMA")
-    ap.add_argument("--waves", type=int, default=0,
+    ap.add_argument("--waves", type=int, default=2,
                     help="run the step through the wave pipeline with this many waves (0: serial calls)")
     ap.add_argument("--split-qkv", action="store_true",
                     help="orthogonalise Q, K and V blocks of fused QKV projections separately")
@@ -345,9 +345,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     pipe = None
-    if args.waves > 0:
-        if args.split_qkv:
-            raise SystemExit("--waves and --split-qkv do not combine")
+    if args.waves > 0 and not args.split_qkv:
         pipe = nsg.ns_pipeline_create(plan, args.waves)
         ws = torch.empty(pipe.workspace_bytes, dtype=torch.uint8, device=dev)
 
