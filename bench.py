@@ -498,9 +498,16 @@ def run_ours(args):
     flops_per_launch = fl[dom] / launches_per_step
     achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
     useful = sum(fl.values())
+    # the recorded traffic is for one launch over the whole 24-layer GPT-style
+    # workload (one NS step of one phase); scale it by this launch's share of
+    # that work (waves split a phase into several launches)
+    traffic = traffic_for(dom, args.gemm_cluster) if args.workload == "gpt" and not args.layers \
+        and not args.split_qkv else None
+    if traffic is not None:
+        traffic = int(traffic * flops_per_launch / (fl[dom] / workloads.STEPS))
     roofline = {"bound": "tensor", "kernel": gemm_kernel_for(dom, args.gemm_cluster)[0], "achieved": achieved,
                 "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
-                "traffic": traffic_for(dom, args.gemm_cluster),
+                "traffic": traffic,
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); burst {burst}",
                 "flops_per_launch": flops_per_launch, "avg_launch_ms": per_launch_ms}
     per_kernel = {k: {"launches_per_step": launches[k] / args.steps, "ms_per_step": kms[k] / args.steps}

@@ -179,3 +179,89 @@ def test_wave_pipeline_equals_serial_step(n_waves):
         y = ho2[homes[i]][ho[i]:ho[i] + ts[i].numel()].reshape(ts[i].shape)
         from gpu_util import BF16_TOL, oracle_ns, rel_err
         assert rel_err(y, oracle_ns(ts[i])) <= BF16_TOL
+
+
+def _e2e_check(plan, shapes, ts, rank_in, S, participating, pipe_waves=0):
+    from gpu_util import BF16_TOL, oracle_ns, rel_err
+    dev = torch.device("cuda:0")
+    homes = plan.homes()
+    ho, hs, rs = plan.home_layout()
+    home_in = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    home_out = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    rank_out = [torch.full_like(x, 5.0) for x in rank_in]
+    if pipe_waves:
+        pipe = nsg.ns_pipeline_create(plan, pipe_waves)
+        ws = torch.empty(pipe.workspace_bytes, dtype=torch.uint8, device=dev)
+        nsg.ns_pipeline_run(pipe, rank_in, home_in, home_out, rank_out, ws)
+    else:
+        part = [i for i in range(len(shapes)) if participating[i]]
+        ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+        ins = [home_in[homes[i]].data_ptr() + 2 * ho[i] for i in part]
+        outs = [home_out[homes[i]].data_ptr() + 2 * ho[i] for i in part]
+        nsg.ns_pack_to_home(plan, rank_in, home_in)
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+        nsg.ns_unpack_from_home(plan, home_out, rank_out)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for i, t in enumerate(ts):
+        if not participating[i]:
+            continue
+        y = home_out[homes[i]][ho[i]:ho[i] + t.numel()].reshape(t.shape)
+        assert rel_err(y, oracle_ns(t)) <= BF16_TOL, i
+    return home_out, rank_out
+
+
+@pytest.mark.parametrize("waves", [0, 3])
+def test_flat_model_pack_ns_unpack(waves):
+    # owner_planning data model end to end: a flat buffer with 1-D (ineligible)
+    # and padded gaps, owners by the default balancer
+    g = np.random.default_rng(5)
+    shapes, offsets, pos = [], [], 0
+    for k in range(14):
+        shp = (int(g.integers(8, 60)),) if k % 5 == 4 else (int(g.integers(16, 300)), int(g.integers(16, 300)))
+        pos += int(g.integers(0, 9))
+        offsets.append(pos)
+        shapes.append(shp)
+        pos += int(np.prod(shp))
+    S = 4
+    size = ((pos + S - 1) // S) * S
+    dev = torch.device("cuda:0")
+    flat = torch.zeros(size, dtype=torch.bfloat16)
+    ts = []
+    for i, (s, off) in enumerate(zip(shapes, offsets)):
+        t = workloads.gen_tensor(s, 1.0, 95, i)
+        ts.append(t)
+        flat[off:off + t.numel()] = t.reshape(-1)
+    per = size // S
+    rank_in = [flat[r * per:(r + 1) * per].clone().to(dev) for r in range(S)]
+    plan = nsg.ns_plan_create_flat(shapes, offsets, size, S=S)
+    part = [len(s) >= 2 for s in shapes]
+    home_out, rank_out = _e2e_check(plan, shapes, ts, rank_in, S, part, waves)
+    # the scatter puts every result back at its flat position; others keep 5.0
+    back = torch.cat([x.cpu() for x in rank_out])
+    for i, (t, off) in enumerate(zip(ts, offsets)):
+        if part[i]:
+            homes = plan.homes()
+            ho, _, _ = plan.home_layout()
+            want = home_out[homes[i]][ho[i]:ho[i] + t.numel()].cpu()
+            assert torch.equal(back[off:off + t.numel()], want)
+        else:
+            assert torch.all(back[off:off + t.numel()] == 5.0)
+
+
+@pytest.mark.parametrize("waves", [0, 2])
+def test_two_stage_model_pack_ns_unpack(waves):
+    shapes = [(512, 256), (256, 512, 2), (1024, 128), (256, 64, 4)]
+    pd = [1, 1, 0, 2]
+    R, T = 2, 2
+    ts = workloads.gen_tensors(workloads.Workload("tsn", shapes, 1.0, 96))
+    np_ts = [bits(t).reshape(t.shape) for t in ts]
+    dev = torch.device("cuda:0")
+    ranks = orr.make_rank_buffers_two_stage(np_ts, R, T, pd)
+    rank_in = [torch.from_numpy(r.view(np.int16).copy()).view(torch.bfloat16).to(dev) for r in ranks]
+    plan = nsg.ns_plan_create_two_stage(shapes, pd, R, T)
+    home_out, rank_out = _e2e_check(plan, shapes, ts, rank_in, R * T, [True] * len(shapes), waves)
+    # unpack: every rank gets its two-stage piece of every result
+    homes = plan.homes()
+    full = orr.route_two_stage_back([bits(h) for h in home_out], shapes, pd, dict(enumerate(homes)), R, T)
+    for r in range(R * T):
+        assert np.array_equal(bits(rank_out[r]), full[r][:rank_out[r].numel()])
