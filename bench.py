@@ -115,20 +115,21 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def gemm_kernel_for(kind: str, cluster_mode: int):
+def gemm_kernel_for(kind: str, cluster_mode: int, shapes=()):
     """(kernel name, source file) of the GEMM kind under a tiling mode: the
-    library's default runs the 2-SM kernel for Gram and B*X, the 1-SM kernel
-    for A*A."""
-    mode = cluster_mode if cluster_mode else (1 if kind == "a2b" else 3)
+    library's default runs the 2-SM kernel for Gram and, when every bucket has
+    an even number of 128-row tile rows, for B*X; the 1-SM kernel for A*A."""
+    even = all(((view_mn(s)[0] + 127) // 128) % 2 == 0 for s in shapes)
+    mode = cluster_mode if cluster_mode else (1 if kind == "a2b" or (kind == "bx" and not even) else 3)
     if mode == 3:
         return f"ns_gemm2sm_kernel<{kind}>", "gemm2sm.cu"
     return f"ns_gemm_kernel<{kind}>", "gemm.cu"
 
 
-def traffic_for(kind: str, cluster_mode: int):
+def traffic_for(kind: str, cluster_mode: int, shapes=()):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current source of that kernel (else None)."""
-    name, fname = gemm_kernel_for(kind, cluster_mode)
+    name, fname = gemm_kernel_for(kind, cluster_mode, shapes)
     src = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc", fname)
     summ = os.path.join(ROOT, "profiles", "gemm_traffic.md")
     try:
@@ -501,11 +502,11 @@ def run_ours(args):
     # the recorded traffic is for one launch over the whole 24-layer GPT-style
     # workload (one NS step of one phase); scale it by this launch's share of
     # that work (waves split a phase into several launches)
-    traffic = traffic_for(dom, args.gemm_cluster) if args.workload == "gpt" and not args.layers \
+    traffic = traffic_for(dom, args.gemm_cluster, ns_shapes) if args.workload == "gpt" and not args.layers \
         and not args.split_qkv else None
     if traffic is not None:
         traffic = int(traffic * flops_per_launch / (fl[dom] / workloads.STEPS))
-    roofline = {"bound": "tensor", "kernel": gemm_kernel_for(dom, args.gemm_cluster)[0], "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": gemm_kernel_for(dom, args.gemm_cluster, ns_shapes)[0], "achieved": achieved,
                 "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
                 "traffic": traffic,
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); burst {burst}",
