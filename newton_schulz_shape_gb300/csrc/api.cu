@@ -131,17 +131,22 @@ int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out) {
 }
 
 // 3-D bf16 tensor map over [count][outer][inner] with a {box_inner, box_outer, 1}
-// box, 128-byte swizzle, zero fill outside the array.
+// box, 128-byte swizzle (operand tiles) or 64-byte swizzle (epilogue chunks of
+// 32 x 32), zero fill outside the array.
 int make_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count, uint32_t box_inner,
-             uint32_t box_outer) {
+             uint32_t box_outer, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[3] = {inner, outer, count};
   cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
   cuuint32_t box[3] = {box_inner, box_outer, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
+}
+
+int make_epi_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count) {
+  return make_map(m, base, inner, outer, count, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Upper-triangle work items of one matrix: single tiles (cl = 1) or pairs of
@@ -222,6 +227,8 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
     char* nxt = cur_is_x0 ? q.x1 : q.x0;
     const uint64_t cnt = b.members.size();
     nsk::GemmBucket& g = gp.bk[nb];
+    // output maps exist in the parameter blocks of launches that store by TMA
+    CUtensorMap* tmo = sizeof(gp.tmo) / sizeof(gp.tmo[0]) > 1 ? &gp.tmo[nb] : nullptr;
     g.tile_begin = tiles;
     g.count = static_cast<int>(cnt);
     g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
@@ -240,6 +247,7 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
         g.aux = nullptr;
         rc = make_map(&gp.tma[nb], cur, b.n_pad, b.m_pad, cnt, 64, 128);
         if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 128);
+        if (rc == NS_OK) rc = tmo ? make_epi_map(tmo, q.a, b.m_pad, b.m_pad, cnt) : NS_ERR_UNSUPPORTED;
       } else {
         g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM_BK);
         g.out = q.b;
@@ -248,6 +256,8 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
         g.aux_stride = b.m_pad * b.m_pad;
         rc = make_map(&gp.tma[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
         if (rc == NS_OK) rc = make_map(&gp.tmb[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
+        if (rc == NS_OK) rc = make_epi_map(&gp.tme[nb], q.a, b.m_pad, b.m_pad, cnt);
+        if (rc == NS_OK) rc = tmo ? make_epi_map(tmo, q.b, b.m_pad, b.m_pad, cnt) : NS_ERR_UNSUPPORTED;
       }
     } else {
       g.tiles_n = static_cast<int>((b.n_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
@@ -262,6 +272,8 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
       g.aux_stride = b.m_pad * b.n_pad;
       rc = make_map(&gp.tma[nb], q.b, b.m_pad, b.m_pad, cnt, 64, 128);
       if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 64);
+      if (rc == NS_OK) rc = make_epi_map(&gp.tme[nb], cur, b.n_pad, b.m_pad, cnt);
+      if (rc == NS_OK && !final_out) rc = tmo ? make_epi_map(tmo, nxt, b.n_pad, b.m_pad, cnt) : NS_ERR_UNSUPPORTED;
       if (final_out) {
         g.out_first = n_out;
         for (size_t s = 0; s < cnt; ++s) {

@@ -25,6 +25,7 @@
 
 #include <algorithm>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -43,7 +44,7 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + EPI_RING_BYTES + 512;
 
 template <int PHASE, typename P>
 __device__ __forceinline__ void decode_pair(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
@@ -74,37 +75,24 @@ __device__ __forceinline__ void decode_pair(const P& p, long long t, uint32_t ra
   tm = 2 * q + static_cast<int>(rank);
 }
 
-__device__ __forceinline__ uint32_t pack2bf(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void unpack8(const uint4& q, float* f) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = __uint_as_float(w[k] << 16);
-    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-  }
-}
-
 template <int PHASE, bool FINAL, typename P>
 __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_constant__ P p) {
   static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
   constexpr bool B_MN = (PHASE == PH_BX);
-  constexpr bool SYRK = (PHASE != PH_BX);
   constexpr uint32_t IDESC = idesc_make(1u, 2 * BM, BN, false, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* ring = smem + STAGES * STAGE_BYTES;  // epilogue chunk slots
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + EPI_RING_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rfull = drain + 1;  // EPI_WARPS x EPI_SLOTS
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + EPI_WARPS * EPI_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (blockDim.x != THREADS) {
@@ -128,11 +116,14 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       mbar_init(&tempty[a], 8);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < EPI_WARPS * EPI_SLOTS; ++i) mbar_init(&rfull[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     for (int b = 0; b < p.nb; ++b) {
       prefetch_tmap(&p.tma[b]);
       prefetch_tmap(&p.tmb[b]);
+      if (PHASE != PH_GRAM) prefetch_tmap(&p.tme[b]);
+      if (!FINAL) prefetch_tmap(&p.tmo[b]);
     }
   }
   // the collective 2-SM TMEM allocation needs the peer CTA running: meet first
@@ -223,109 +214,13 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
   } else if (warp >= 2) {
     // -------------------------------------------------------------- epilogue
     const int lg = warp & 3;
-    uint32_t acc = 0, acc_phase = 0;
-    for (long long t = t0; t < p.total_tiles; t += tstride) {
-      int b, mat, tm, tn;
+    auto dec = [&](long long t, int& b, int& mat, int& tm, int& tn) {
       decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
-      const GemmBucket& B = p.bk[b];
-      const int cend = tm < B.tiles_m ? BN : 0;  // the spare half of an odd last pair stores nothing
-      const int r0w = tm * BM + lg * 32;
-      const int r = r0w + lane;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(mat) * B.out_stride;
-      const __nv_bfloat16* aux =
-          reinterpret_cast<const __nv_bfloat16*>(B.aux) + static_cast<long long>(mat) * B.aux_stride;
-      uint4 ax[BN / 32][4];
-      if (PHASE != PH_GRAM) {
-#pragma unroll
-        for (int ci = 0; ci < BN / 32; ++ci) {
-          const int cg = tn * BN + ci * 32;
-          if (ci * 32 < cend && cg < B.cols_valid && !(SYRK && cg + 31 < r0w)) {
-            const uint4* src = reinterpret_cast<const uint4*>(aux + static_cast<long long>(r) * B.ld_aux + cg);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ax[ci][q] = __ldcg(src + q);
-          }
-        }
-      }
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int ci = 0; ci < BN / 32; ++ci) {
-        const int c0 = ci * 32;
-        if (c0 >= cend) break;
-        const int cg = tn * BN + c0;
-        if (cg >= B.cols_valid) break;
-        if (SYRK && cg + 31 < r0w) continue;
-        uint32_t v[32];
-        tmem_ld32(tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + acc * BN + c0, v);
-        tmem_ld_wait();
-        float f[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-        if (PHASE != PH_GRAM) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float x[8];
-            unpack8(ax[ci][q], x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              if (PHASE == PH_A2B)
-                f[q * 8 + e] = p.beta * x[e] + p.gamma * f[q * 8 + e];
-              else
-                f[q * 8 + e] = p.alpha * x[e] + f[q * 8 + e];
-            }
-          }
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack2bf(f[2 * j], f[2 * j + 1]);
-        const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(w);
-        if (FINAL) {
-          if (r < B.m_valid) {
-            const unsigned long long e = p.out_tab[B.out_first + mat];
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e & ~1ull);
-            if (!(e & 1ull)) {
-              __nv_bfloat16* dst = o + static_cast<long long>(r) * B.n_valid + cg;
-              if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (cg + j < B.n_valid) dst[j] = hv[j];
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (cg + j < B.n_valid) o[static_cast<long long>(cg + j) * B.m_valid + r] = hv[j];
-            }
-          }
-          continue;
-        }
-        __nv_bfloat16* dst = out + static_cast<long long>(r) * B.ld_out + cg;
-        if (!SYRK || cg >= r) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (cg + j >= r) dst[j] = hv[j];
-        }
-        if (SYRK) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = cg + j;
-            if (c > r) out[static_cast<long long>(c) * B.ld_out + r] = hv[j];
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
-    }
+    };
+    // the leader's MMA waits for all 8 epilogue warps of the pair
+    auto release = [&](uint32_t a) { mbar_arrive_cluster(map_to_rank(&tempty[a], 0)); };
+    epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, tfull,
+                                ring + lg * EPI_SLOTS * EPI_SLOT_BYTES, rfull + lg * EPI_SLOTS, abort_flag);
   }
 
   tc_fence_before();

@@ -39,6 +39,10 @@ template <int NOUT>
 struct GemmParamsT {
   CUtensorMap tma[GEMM_MAX_BUCKETS];  // A operand, K-major, box {64, 128, 1}
   CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} / MN-major box {64,64,1}
+  // epilogue chunks, box {32, 32, 1}, 64-byte swizzle: aux (A2B: A, BX: X)
+  // and output (final-store launches write from registers: no output map)
+  CUtensorMap tme[GEMM_MAX_BUCKETS];
+  CUtensorMap tmo[NOUT == 1 ? GEMM_MAX_BUCKETS : 1];
   GemmBucket bk[GEMM_MAX_BUCKETS];
   long long total_tiles;
   int nb;
