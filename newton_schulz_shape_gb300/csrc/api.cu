@@ -212,7 +212,7 @@ BucketPtrs bucket_ptrs(const Bucket& b, char* ws) {
 // entry is the output address with bit 0 set for transposed tensors.
 template <typename P>
 int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1,
-               unsigned int* status, void* const* final_out, int cl) {
+               unsigned int* status, void* const* final_out, int cl, bool first_step) {
   std::memset(&gp, 0, sizeof(gp));
   gp.alpha = p.a;
   gp.beta = p.b;
@@ -234,6 +234,8 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
     g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
     g.m_valid = static_cast<int>(b.m);
     g.n_valid = static_cast<int>(b.n);
+    // X~_0 is unscaled: the first step's Gram and B*X apply the scale
+    g.scale = first_step && phase != nsk::PH_A2B ? q.scale : nullptr;
     int rc = NS_OK;
     if (phase == nsk::PH_GRAM || phase == nsk::PH_A2B) {
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
@@ -292,10 +294,10 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
 }
 
 int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
-              unsigned int* status, cudaStream_t st) {
+              unsigned int* status, bool first_step, cudaStream_t st) {
   nsk::GemmParams gp;
   const int cl = pick_cl(p, b0, b1, phase);
-  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl));
+  int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl), first_step);
   if (rc != NS_OK) return rc;
   return counted(phase, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, cl, gp, nsm, st);
@@ -306,10 +308,10 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
 
 // B*X phase of the last step, storing results directly into `out`.
 int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
-                 void* const* out, cudaStream_t st) {
+                 void* const* out, bool first_step, cudaStream_t st) {
   static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
   const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
-  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl));
+  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step);
   if (rc != NS_OK) return rc;
   return counted(nsk::PH_BX, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(cl, gp, nsm, st);
@@ -874,7 +876,8 @@ int orthogonalize_f32(const Plan& p, const void* const* in, void* const* out, ch
 // zero padded into the workspace.
 int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* ws, unsigned int* status,
                   cudaStream_t st) {
-  // prologue: sums of squares, scales, X_0 = scale * (T or T^T), zero padded
+  // prologue: X~_0 = T or T^T (unscaled, zero padded) with per-stripe sums of
+  // squares in one pass, then the scales
   for (const Bucket& b : p.buckets) {
     const BucketPtrs q = bucket_ptrs(b, ws);
     const size_t cnt = b.members.size();
@@ -904,9 +907,8 @@ int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* 
         d.cols = static_cast<int>(t.cols);
         d.transposed = t.transposed ? 1 : 0;
       }
-      if (counted(K_PRO, st, [&] { return nsk::launch_sumsq(pp, st); }) != cudaSuccess ||
-          counted(K_PRO, st, [&] { return nsk::launch_scale(pp, st); }) != cudaSuccess ||
-          counted(K_PRO, st, [&] { return nsk::launch_prep(pp, st); }) != cudaSuccess)
+      if (counted(K_PRO, st, [&] { return nsk::launch_prep(pp, st); }) != cudaSuccess ||
+          counted(K_PRO, st, [&] { return nsk::launch_scale(pp, st); }) != cudaSuccess)
         return NS_ERR_CUDA;
     }
   }
@@ -927,10 +929,10 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
       for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
         const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
         if (last && phase == nsk::PH_BX && group_matrices(p, b0, b1) <= size_t(nsk::GEMM_MAX_OUT)) {
-          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, st);
+          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, st);
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
-          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, st);
+          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, st);
         }
         if (rc != NS_OK) return rc;
       }
@@ -953,12 +955,14 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
       pp.m = static_cast<int>(b.m);
       pp.n = static_cast<int>(b.n);
       pp.out_f32 = p.out_bytes == 4 ? 1 : 0;
+      pp.apply_scale = p.steps == 0 ? 1 : 0;  // X~_0 itself, still unscaled
       pp.status = status;
       for (int k = 0; k < pp.count; ++k) {
         const size_t s = s0 + k;
         const Tensor& t = p.t[b.members[s]];
         nsk::MatDesc& d = pp.md[k];
         d.out = out[t.ordinal];
+        d.scale = q.scale + s;
         d.xfinal = xf + s * b.m_pad * b.n_pad * 2;
         d.rows = static_cast<int>(t.rows);
         d.cols = static_cast<int>(t.cols);

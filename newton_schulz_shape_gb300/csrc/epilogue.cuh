@@ -9,6 +9,10 @@
 //   PH_A2B   out = b * aux + c * acc        (B = b A + c A^2, aux = A)
 //   PH_BX    out = a * aux + acc            (X' = a X + B X, aux = X)
 //
+// In the first step X is the unscaled X~_0 and the per-matrix scale
+// s = 1 / (||T||_F + eps) enters here: out = s^2 acc (Gram) and
+// out = s (a aux + acc) (B*X), i.e. the step run on X_0 = s X~_0.
+//
 // Data movement is staged through shared memory so that global memory only
 // sees whole rows of a chunk:
 //   * every warp has a ring of EPI_SLOTS chunk slots (32 rows x 64 bytes,
@@ -142,6 +146,8 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
     }
     const int r0w = e.tm * GEMM_BM + lg * 32;
     const int r = r0w + lane;
+    // first step: X~_0 is unscaled, s = 1 / (||T||_F + eps) per matrix
+    const float sc = (PHASE != PH_A2B && B.scale) ? B.scale[e.mat] : 1.0f;
     for (int ci = e.ci_lo; ci < e.ci_hi; ++ci, ++g) {
       const int s = static_cast<int>(g % EPI_SLOTS);
       uint8_t* slot = ring + s * EPI_SLOT_BYTES;
@@ -169,6 +175,11 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
       float f[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+      if (PHASE == PH_GRAM) {
+        const float sc2 = sc * sc;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] *= sc2;
+      }
       if (AUX) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -183,8 +194,8 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
               f0 = p.beta * x0 + p.gamma * f0;
               f1 = p.beta * x1 + p.gamma * f1;
             } else {
-              f0 = p.alpha * x0 + f0;
-              f1 = p.alpha * x1 + f1;
+              f0 = sc * (p.alpha * x0 + f0);
+              f1 = sc * (p.alpha * x1 + f1);
             }
           }
         }

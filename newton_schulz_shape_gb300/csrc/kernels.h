@@ -28,12 +28,15 @@ struct GemmBucket {
   int cols_valid;        // output columns that exist (m_pad or n_pad)
   int m_valid, n_valid;  // unpadded m, n (final-store launches)
   int out_first;         // first entry of this bucket in out_tab (final-store launches)
+  const float* scale;    // first step's Gram and B*X: per-matrix 1 / (||T||_F + eps), X~_0
+                         // being unscaled (Gram: out = s^2 acc; B*X: out = s (a aux + acc));
+                         // null otherwise
 };
 
 // Final-store launches of the B*X phase write each result straight to the
 // caller's output tensor; out_tab holds one entry per matrix: the output
 // address with bit 0 set when the tensor was transposed (rows > cols).
-constexpr int GEMM_MAX_OUT = 3584;
+constexpr int GEMM_MAX_OUT = 3520;
 
 template <int NOUT>
 struct GemmParamsT {
@@ -138,6 +141,7 @@ struct ProParams {
   float eps;
   int out_f32;          // result dtype: 0 bf16, 1 fp32
   long long x_split;    // fp32-Gram: elements between the X hi / X lo / X^T hi / X^T lo buffers
+  int apply_scale;      // store: multiply by *scale (bf16 path with zero steps)
   unsigned int* status;
 };
 

@@ -142,7 +142,9 @@ int finish(Plan& p, bool keep_homes = false) {
     b.off_x1 = take(gs ? cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * 3 * aset : xbytes);
     b.off_a = take(abytes);
     b.off_b = take(abytes);
-    b.nchunks = (b.m * b.n + kSumsqChunk - 1) / kSumsqChunk;
+    // partial sums of squares per matrix: 32K-element chunks (fp32 paths) or
+    // 64-row stripes of the padded X_0 (bf16 path)
+    b.nchunks = f32 ? (b.m * b.n + kSumsqChunk - 1) / kSumsqChunk : b.m_pad / 64;
     b.off_partial = take(cnt * uint64_t(b.nchunks) * 4);
     b.off_scale = take(cnt * 4);
     b.off_coef = take(cnt * 3 * 4);

@@ -2,9 +2,10 @@
 // page owner_planning, ns_cost_fn: view as (shape[0], prod(shape[1:])),
 // normalise, transpose so rows <= cols; the result is transposed back).
 //
-//   ns_sumsq_kernel   per-matrix partial sums of squares over 32K-element chunks
+//   ns_prep_kernel    bf16 path: X~_0 = T or T^T, zero-padded to m_pad x n_pad,
+//                     unscaled, and per-stripe partial sums of squares (one pass)
+//   ns_sumsq_kernel   fp32 paths: partial sums of squares over 32K-element chunks
 //   ns_scale_kernel   scale = 1 / (sqrt(sum of partials) + eps), fixed order
-//   ns_prep_kernel    X_0 = scale * (T or T^T), zero-padded to m_pad x n_pad, bf16
 //   ns_store_kernel   out = X_k (or X_k^T) cropped to the tensor's (rows, cols)
 //
 // Each launch covers up to PRO_MAX_MATS matrices of one shape bucket; the
@@ -87,86 +88,135 @@ __global__ void __launch_bounds__(256) ns_scale_kernel(const __grid_constant__ P
   if (threadIdx.x == 0) *d.scale = static_cast<float>(1.0 / (sqrt(red[0]) + static_cast<double>(p.eps)));
 }
 
-// X_0 = scale * V zero-padded to m_pad x n_pad, V = T (rows <= cols) or T^T.
-// Non-transposed: each thread writes 16 bytes (8 bf16) of X_0 per iteration,
-// reading T with 16-byte loads when its rows are 16-byte aligned.
-// Transposed: one 64 x 64 tile per CTA through a conflict-free fp32 tile in
-// shared memory, 16-byte loads of T rows and 16-byte stores of X_0 rows.
-// blockIdx.y selects the matrix.
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(256) ns_prep_kernel(const __grid_constant__ ProParams p) {
+__device__ __forceinline__ float sq8(const uint4& q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+    acc = fmaf(lo, lo, acc);
+    acc = fmaf(hi, hi, acc);
+  }
+  return acc;
+}
+
+// bf16 prologue, one pass: V = T (rows <= cols) or T^T copied unscaled into
+// X~_0 (m_pad x n_pad, zero padded) and the sum of squares of each 64-row
+// stripe of V written to partial[stripe]. The scale 1 / (||T||_F + eps) is
+// applied by the first step's products (A = s^2 X~ X~^T, X_1 = s (a X~ + B X~)),
+// which equals running the step on X_0 = s X~. The input is bf16, so X~_0
+// holds it exactly. blockIdx.x = stripe of 64 rows of X~_0, blockIdx.y = matrix.
+//
+// Plain: 16-byte vectors of T rows to X~_0 rows, four loads in flight per
+// thread. Transposed: the stripe is 64 columns of T, walked in 64 x 64 tiles
+// (64 rows of T x 128 bytes in, 64 rows of X~_0 x 128 bytes out, both whole
+// lines per warp access) through a double-buffered bf16 tile in shared memory
+// (rows of 33 words: conflict-free writes, 2-way reads).
+constexpr int PREP_THREADS = 256;
+
+__global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_constant__ ProParams p) {
   const MatDesc& d = p.md[blockIdx.y];
-  const float s = *d.scale;
-  const unsigned short* src = reinterpret_cast<const unsigned short*>(d.in);
-  uint4* x4 = reinterpret_cast<uint4*>(d.x);
-  const int nv = p.n_pad / 8;  // 16-byte vectors per X_0 row
+  const unsigned short* __restrict__ src = reinterpret_cast<const unsigned short*>(d.in);
+  uint4* __restrict__ x4 = reinterpret_cast<uint4*>(d.x);
+  const int nv = p.n_pad / 8;  // 16-byte vectors per X~_0 row
+  const int i0 = blockIdx.x * TILE;
+  float acc = 0.0f;
   if (!d.transposed) {
     const bool vec = (p.n % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
-    const long long total = static_cast<long long>(p.m_pad) * nv;
-    for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
-         v += static_cast<long long>(gridDim.x) * blockDim.x) {
-      const int i = static_cast<int>(v / nv);
-      const int j0 = static_cast<int>(v % nv) * 8;
-      float f[8];
-      if (i < p.m && vec && j0 + 8 <= p.n) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(i) * p.n + j0));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const int total = TILE * nv;
+    constexpr int U = 4;
+    for (int base = threadIdx.x; base < total; base += U * PREP_THREADS) {
+      uint4 q[U];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          f[2 * k] = __uint_as_float(w[k] << 16);
-          f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      for (int u = 0; u < U; ++u) {
+        const int v = base + u * PREP_THREADS;
+        const int i = i0 + v / nv, j0 = (v % nv) * 8;
+        q[u] = make_uint4(0, 0, 0, 0);
+        if (v < total && i < p.m) {
+          if (vec && j0 + 8 <= p.n) {
+            q[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(i) * p.n + j0));
+          } else if (j0 < p.n) {
+            uint16_t h[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = j0 + k < p.n ? src[static_cast<long long>(i) * p.n + j0 + k] : 0;
+            q[u] = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                              h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+          }
         }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          f[k] = (i < p.m && j0 + k < p.n) ? bf16_to_f(src[static_cast<long long>(i) * p.n + j0 + k]) : 0.0f;
       }
-      x4[v] = make_uint4(pack2(s * f[0], s * f[1]), pack2(s * f[2], s * f[3]), pack2(s * f[4], s * f[5]),
-                         pack2(s * f[6], s * f[7]));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = base + u * PREP_THREADS;
+        if (v < total) {
+          acc += sq8(q[u]);
+          x4[static_cast<long long>(i0) * nv + v] = q[u];
+        }
+      }
     }
   } else {
-    // V[i][j] = T[j][i], T row-major n x m. Tile (ti, tj) of X_0.
-    __shared__ float tile[TILE][TILE + 1];
-    const int tiles_n = p.n_pad / TILE;
-    const int ti = blockIdx.x / tiles_n, tj = blockIdx.x % tiles_n;
-    const int i0 = ti * TILE, j0 = tj * TILE;
+    // X~[i][j] = T[j][i], T row-major n x m (rows j, cols i)
+    __shared__ uint32_t tile[2][TILE][TILE / 2 + 1];
     const bool vec = (p.m % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
-    // load: 64 rows j of T x 8 vectors of 8 i each; 512 vectors, 2 per thread
-    for (int e = threadIdx.x; e < TILE * 8; e += blockDim.x) {
-      const int jj = e / 8, iv = (e % 8) * 8;
-      const int j = j0 + jj, i = i0 + iv;
-      float f[8];
-      if (j < p.n && vec && i + 8 <= p.m) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(j) * p.m + i));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const int ntiles = p.n_pad / TILE;
+    // each thread moves two 16-byte vectors per tile: vector q = threadIdx.x + 256 h
+    auto load = [&](int jt, uint4 (&r)[2]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = threadIdx.x + h * PREP_THREADS;
+        const int j = jt * TILE + q / 8, i = i0 + (q % 8) * 8;
+        r[h] = make_uint4(0, 0, 0, 0);
+        if (j < p.n && i < p.m) {
+          if (vec && i + 8 <= p.m) {
+            r[h] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(j) * p.m + i));
+          } else {
+            uint16_t e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) e[k] = i + k < p.m ? src[static_cast<long long>(j) * p.m + i + k] : 0;
+            r[h] = make_uint4(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16),
+                              e[4] | (uint32_t(e[5]) << 16), e[6] | (uint32_t(e[7]) << 16));
+          }
+        }
+      }
+    };
+    uint4 r[2];
+    load(0, r);
+    for (int jt = 0; jt < ntiles; ++jt) {
+      const int buf = jt & 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = threadIdx.x + h * PREP_THREADS;
+        const int jj = q / 8, iw = (q % 8) * 4;  // row jj of the tile, word iw (= column 2 iw)
+        acc += sq8(r[h]);
+        tile[buf][jj][iw] = r[h].x;
+        tile[buf][jj][iw + 1] = r[h].y;
+        tile[buf][jj][iw + 2] = r[h].z;
+        tile[buf][jj][iw + 3] = r[h].w;
+      }
+      __syncthreads();
+      if (jt + 1 < ntiles) load(jt + 1, r);  // next tile's loads overlap this tile's stores
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = threadIdx.x + h * PREP_THREADS;
+        const int ii = q / 8, jv = (q % 8) * 8;  // row ii of X~_0's tile, columns jv..jv+7
+        const unsigned short* t16 = reinterpret_cast<const unsigned short*>(&tile[buf][0][0]);
+        uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          f[2 * k] = __uint_as_float(w[k] << 16);
-          f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          const uint32_t lo = t16[(jv + 2 * k) * (TILE + 2) + ii];
+          const uint32_t hi = t16[(jv + 2 * k + 1) * (TILE + 2) + ii];
+          w[k] = lo | (hi << 16);
         }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          f[k] = (j < p.n && i + k < p.m) ? bf16_to_f(src[static_cast<long long>(j) * p.m + i + k]) : 0.0f;
+        x4[(static_cast<long long>(i0 + ii) * p.n_pad + jt * TILE + jv) / 8] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) tile[jj][iv + k] = f[k];
-    }
-    __syncthreads();
-    // store: 64 rows i of X_0 x 8 vectors of 8 j
-    for (int e = threadIdx.x; e < TILE * 8; e += blockDim.x) {
-      const int ii = e % TILE, jv = (e / TILE) * 8;
-      float f[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) f[k] = s * tile[jv + k][ii];
-      x4[(static_cast<long long>(i0 + ii) * p.n_pad + j0 + jv) / 8] =
-          make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
     }
   }
+  acc = block_sum(acc);
+  if (threadIdx.x == 0) d.partial[blockIdx.x] = acc;
 }
 
 // One 64 x 64 tile of the output (rows x cols) per CTA.
@@ -178,12 +228,13 @@ __global__ void __launch_bounds__(256) ns_store_kernel(const __grid_constant__ P
   const int ti = blockIdx.x / tiles_c, tj = blockIdx.x % tiles_c;
   const int i0 = ti * TILE, j0 = tj * TILE;
   const unsigned short* x = reinterpret_cast<const unsigned short*>(d.xfinal);
+  const float sc = p.apply_scale ? *d.scale : 1.0f;  // zero steps: X~_0 is stored unscaled
   const int tx = threadIdx.x % TILE, ty = threadIdx.x / TILE;
   if (!d.transposed) {
     for (int ii = ty; ii < TILE; ii += 4) {
       const int i = i0 + ii, j = j0 + tx;
       if (i < rows && j < cols) {
-        const float v = bf16_to_f(x[static_cast<long long>(i) * p.n_pad + j]);
+        const float v = sc * bf16_to_f(x[static_cast<long long>(i) * p.n_pad + j]);
         if (p.out_f32)
           reinterpret_cast<float*>(d.out)[static_cast<long long>(i) * cols + j] = v;
         else
@@ -195,7 +246,7 @@ __global__ void __launch_bounds__(256) ns_store_kernel(const __grid_constant__ P
     for (int jj = ty; jj < TILE; jj += 4) {
       const int j = j0 + jj, i = i0 + tx;
       float v = 0.0f;
-      if (i < rows && j < cols) v = bf16_to_f(x[static_cast<long long>(j) * p.n_pad + i]);
+      if (i < rows && j < cols) v = sc * bf16_to_f(x[static_cast<long long>(j) * p.n_pad + i]);
       tile[jj][tx] = v;
     }
     __syncthreads();
@@ -329,10 +380,9 @@ cudaError_t launch_scale(const ProParams& p, cudaStream_t st) {
 
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
-  // one CTA per 64 x 64 tile (the transposed path needs exactly that grid; the
-  // plain path grid-strides over the same number of CTAs)
-  const int tiles = (p.m_pad / TILE) * (p.n_pad / TILE);
-  ns_prep_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  // one CTA per 64-row stripe of X~_0 (p.nchunks stripes per matrix)
+  if (p.nchunks != p.m_pad / TILE) return cudaErrorInvalidValue;
+  ns_prep_kernel<<<dim3(p.m_pad / TILE, p.count), PREP_THREADS, 0, st>>>(p);
   return cudaGetLastError();
 }
 
