@@ -117,10 +117,10 @@ def peaks():
 
 def gemm_kernel_for(kind: str, cluster_mode: int, shapes=()):
     """(kernel name, source file) of the GEMM kind under a tiling mode: the
-    library's default runs the 2-SM kernel for Gram and, when every bucket has
-    an even number of 128-row tile rows, for B*X; the 1-SM kernel for A*A."""
+    library's default runs the 2-SM kernel for Gram, and for A*A and B*X when
+    every bucket has an even number of 128-row tile rows (else the 1-SM one)."""
     even = all(((view_mn(s)[0] + 127) // 128) % 2 == 0 for s in shapes)
-    mode = cluster_mode if cluster_mode else (1 if kind == "a2b" or (kind == "bx" and not even) else 3)
+    mode = cluster_mode if cluster_mode else (3 if kind == "gram" or even else 1)
     if mode == 3:
         return f"ns_gemm2sm_kernel<{kind}>", "gemm2sm.cu"
     return f"ns_gemm_kernel<{kind}>", "gemm.cu"
@@ -470,6 +470,9 @@ def run_ours(args):
 
         e2e_steps(2)                                    # warm-up of the pipeline
         barrier()
+        e2e_clocks = ClockSampler(uuid)
+        e2e_clocks.start()
+        time.sleep(0.3)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -480,6 +483,7 @@ def run_ours(args):
         stream.wait_stream(s_in)
         e1.record(stream)
         barrier()
+        clk_e2e = e2e_clocks.stop()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
         # the results of the last step really came back
         ok = all(torch.equal(hout[(args.steps - 1) % 2][r], rank_out[r].cpu()) for r in range(S))
@@ -487,7 +491,7 @@ def run_ours(args):
         e2e = {"value": job_value(n_mats, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "pipelining": "copies of step k+1 (in) and k-1 (out) overlap step k's compute",
-               "results_returned": ok, "copy_gbs": copy_gbs}
+               "results_returned": ok, "copy_gbs": copy_gbs, "clocks": clk_e2e}
 
     # ---- roofline of the dominant kernel
     burst, sustained, hbm, peak_src = peaks()

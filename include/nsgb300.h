@@ -266,9 +266,9 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * 128 x 256 tile (tcgen05 cta_group::1); cl = 2: clusters of two such CTAs
  * sharing each B tile by TMA multicast; cl = 3: clusters of two CTAs running
  * the 2-SM MMA (cta_group::2) on 256 x 256 tiles, each SM holding half of
- * each operand; cl = 0 (default) picks 3 for the Gram phase, 3 for B*X when
- * every bucket has an even number of 128-row tile rows (else 1), and 1 for
- * A*A (the fastest measured per phase). Paired modes apply to launches
+ * each operand; cl = 0 (default) picks 3 for the Gram phase, and 3 for A*A
+ * and B*X when every bucket has an even number of 128-row tile rows (else 1):
+ * the fastest measured per phase. Paired modes apply to launches
  * whose buckets all have at least two 128-row tile rows; others use 1.
  * Process-wide; all modes give bitwise-identical results. */
 int ns_set_gemm_cluster(int cl);
