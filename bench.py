@@ -130,10 +130,12 @@ def traffic_for(kind: str, cluster_mode: int, shapes=()):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current source of that kernel (else None)."""
     name, fname = gemm_kernel_for(kind, cluster_mode, shapes)
-    src = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc", fname)
+    csrc = os.path.join(ROOT, "newton_schulz_shape_gb300", "csrc")
     summ = os.path.join(ROOT, "profiles", "gemm_traffic.md")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        # the kernel's own file and the epilogue it includes
+        sha = hashlib.sha256(b"".join(open(os.path.join(csrc, f), "rb").read()
+                                      for f in (fname, "epilogue.cuh"))).hexdigest()[:16]
         for line in open(summ):
             if line.startswith("traffic:"):
                 kv = dict(x.strip().split("=", 1) for x in line[len("traffic:"):].split(";") if "=" in x)
