@@ -60,6 +60,10 @@ def parse():
                     help="orthogonalise Q, K and V blocks of fused QKV projections separately")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-budget", type=float, default=20.0,
+                    help="seconds of oracle work per cpu_baseline / reference sample")
+    ap.add_argument("--no-1thread", action="store_true",
+                    help="skip the single-thread oracle run reported beside cpu_baseline")
     return ap.parse_args()
 
 
@@ -103,6 +107,32 @@ def flops_by_kind(shapes, k):
         a2 += 2 * m * m * m * k
         bx += 2 * m * m * n * k
     return {"gram": g, "a2b": a2, "bx": bx}
+
+
+# NVIDIA's dense (no 2:4 sparsity) bf16 tensor-core figure for one GB300 GPU
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def executed_flops_by_kind(shapes, k, cluster_mode: int = 0):
+    """Tensor-core flops the kernels execute per call, by kind: whole tiles on
+    the zero-padded operands, only the upper tiles of the symmetric products,
+    spare half pairs of odd tile-row counts included. Useful flops
+    (flops_by_kind) can exceed the tensor-pipe rate because SYRK skips work."""
+    ex = {"gram": 0, "a2b": 0, "bx": 0}
+    for s in shapes:
+        m, n = view_mn(s)
+        m_pad, n_pad = -(-m // 128) * 128, -(-n // 64) * 64
+        tm, tn_sym, tn_bx = m_pad // 128, -(-m_pad // 256), -(-n_pad // 256)
+        for kind, kdim in (("gram", n_pad), ("a2b", m_pad), ("bx", m_pad)):
+            mode = int(gemm_kernel_for(kind, cluster_mode, shapes)[0].startswith("ns_gemm2sm")) if tm >= 2 else 0
+            if kind == "bx":
+                tiles = (-(-tm // 2) * 2 if mode else tm) * tn_bx
+            elif mode:
+                tiles = 2 * sum(tn_sym - q for q in range(-(-tm // 2)))
+            else:
+                tiles = sum(tn_sym - (r * 128) // 256 for r in range(tm))
+            ex[kind] += 2 * 128 * 256 * kdim * tiles * k
+    return ex
 
 
 def peaks():
@@ -267,17 +297,48 @@ def cpu_oracle_sample(w, budget_s: float = 20.0):
         "extrapolated by bucket count: " + "; ".join(sample)
 
 
+def blas_threads():
+    try:
+        import threadpoolctl
+        return max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
+    except Exception:
+        return None
+
+
+def oracle_single_thread(args, budget_s: float = 8.0):
+    """The same oracle sample with every BLAS/OpenMP pool limited to one
+    thread (a child process: the limits must be set before numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", args.workload,
+           "--layers", str(args.layers), "--steps", "1", "--warmup", "0", "--no-1thread",
+           "--oracle-budget", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])["value"]
+    except Exception:
+        return None
+
+
+def cpu_baseline_entry(w, args, v, threads, sample):
+    d = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+         "host_cpus": os.cpu_count(), "blas_threads": blas_threads()}
+    if not args.no_1thread:
+        d["value_1thread"] = oracle_single_thread(args)
+    return d
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = get_workload(args.workload, args.layers)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w)
+        cpu_oracle_sample(w, args.oracle_budget)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, threads, sample = cpu_oracle_sample(w)
+        v, threads, sample = cpu_oracle_sample(w, args.oracle_budget)
         vals.append(v)
     wall = time.perf_counter() - t0
     v = statistics.median(vals)
@@ -286,7 +347,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": w.name, "matrices": len(w.shapes), "S": w.S},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "cpu_baseline": cpu_baseline_entry(w, args, v, threads, sample),
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": wall}
     print(json.dumps(line), flush=True)
@@ -516,12 +577,16 @@ def run_ours(args):
                 "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
                 "traffic": traffic,
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); burst {burst}",
+                "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                "useful_tflops_step": useful / (ms_step * 1e-3) / 1e12,
                 "flops_per_launch": flops_per_launch, "avg_launch_ms": per_launch_ms}
     per_kernel = {k: {"launches_per_step": launches[k] / args.steps, "ms_per_step": kms[k] / args.steps}
                   for k in launches}
+    ex = executed_flops_by_kind(ns_shapes, workloads.STEPS, args.gemm_cluster)
     for k in gemm_kinds:
         if kms[k] > 0:
             per_kernel[k]["tflops"] = fl[k] / (kms[k] / args.steps * 1e-3) / 1e12
+            per_kernel[k]["executed_tflops"] = ex[k] / (kms[k] / args.steps * 1e-3) / 1e12
     pack_bytes = 2 * 2 * S * L   # read + write, bf16
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -547,8 +612,8 @@ def run_ours(args):
         "roofline": roofline,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, threads, sample = cpu_oracle_sample(w)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        v, threads, sample = cpu_oracle_sample(w, args.oracle_budget)
+        line["cpu_baseline"] = cpu_baseline_entry(w, args, v, threads, sample)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
