@@ -293,11 +293,12 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
 }
 
 int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
-              unsigned int* status, bool first_step, cudaStream_t st) {
+              unsigned int* status, bool first_step, bool reverse, cudaStream_t st) {
   nsk::GemmParams gp;
   const int cl = pick_cl(p, b0, b1, phase);
   int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl), first_step);
   if (rc != NS_OK) return rc;
+  gp.reverse = reverse ? 1 : 0;
   return counted(phase, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, cl, gp, nsm, st);
          }) == cudaSuccess
@@ -307,10 +308,11 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
 
 // B*X phase of the last step, storing results directly into `out`.
 int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
-                 void* const* out, bool first_step, cudaStream_t st) {
+                 void* const* out, bool first_step, bool reverse, cudaStream_t st) {
   static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
   const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
   int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step);
+  gp.reverse = reverse ? 1 : 0;
   if (rc != NS_OK) return rc;
   return counted(nsk::PH_BX, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(cl, gp, nsm, st);
@@ -927,11 +929,14 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
     for (int phase = nsk::PH_GRAM; phase <= nsk::PH_BX; ++phase) {
       for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
         const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
+        // serpentine order: every other product walks its tiles backwards,
+        // starting on the matrices the previous product wrote last (still in L2)
+        const bool serp = ((step * 3 + phase) & 1) != 0;
         if (last && phase == nsk::PH_BX && group_matrices(p, b0, b1) <= size_t(nsk::GEMM_MAX_OUT)) {
-          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, st);
+          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, serp, st);
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
-          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, st);
+          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, serp, st);
         }
         if (rc != NS_OK) return rc;
       }

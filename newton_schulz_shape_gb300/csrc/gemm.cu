@@ -6,7 +6,10 @@
 //   PH_BX    X' = a X + B X             full tiles, written to the other X buffer
 //
 // One persistent kernel per phase, one CTA per SM, a 128 x 256 output tile per
-// work item, tiles of every shape bucket of the launch in one static schedule.
+// work item, tiles of every shape bucket of the launch in one static schedule,
+// walked first to last or (p.reverse) last to first: successive launches
+// alternate, so each starts on the matrices its predecessor wrote last, which
+// are still in L2.
 // Warp roles (192 threads):
 //   warp 0 lane 0   TMA producer: K-blocks of 64 into a 4-stage smem ring
 //   warp 1          TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=256,
@@ -48,6 +51,7 @@ constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + EPI_RING_BYT
 template <int PHASE, int CL, typename P>
 __device__ __forceinline__ void decode_tile(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
                                             int& tn) {
+  if (p.reverse) t = p.total_tiles - 1 - t;
   b = 0;
   while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
   const GemmBucket& B = p.bk[b];

@@ -49,6 +49,7 @@ constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + EPI_RING_BYT
 template <int PHASE, typename P>
 __device__ __forceinline__ void decode_pair(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
                                             int& tn) {
+  if (p.reverse) t = p.total_tiles - 1 - t;
   b = 0;
   while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
   const GemmBucket& B = p.bk[b];

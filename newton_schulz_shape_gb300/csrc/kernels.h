@@ -50,6 +50,7 @@ struct GemmParamsT {
   long long total_tiles;
   int nb;
   float alpha, beta, gamma;  // a, b, c of the quintic step
+  int reverse;               // walk the tiles last to first (serpentine order across launches)
   unsigned int* status;
   unsigned long long out_tab[NOUT];
 };
