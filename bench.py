@@ -44,9 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt", "small", "llama", "moe", "sweep"], default="gpt")
-    ap.add_argument("--gram", choices=["bf16", "fp32", "fp32gs"], default="bf16",
+    ap.add_argument("--gram", choices=["bf16", "fp32", "fp32gs", "fp32auto"], default="bf16",
                     help="precision policy (sweep workload): bf16 path, fp32-Gram (split TF32) path, "
-                         "or its Gram-space form")
+                         "its Gram-space form, or per bucket the faster of the two (Gram space when n >= 2m)")
     ap.add_argument("--ridge", type=float, default=0.0, help="trace ridge (fp32-Gram path only)")
     ap.add_argument("--points", type=str, default="",
                     help="sweep subset, e.g. '1024x1,4096x8' (m x aspect); default: all")
@@ -636,7 +636,8 @@ def run_sweep(args):
     if args.points:
         want = {tuple(int(x) for x in p.split("x")) for p in args.points.split(",")}
         pts = [p for p in pts if (p[0], p[1]) in want]
-    mode = {"bf16": nsg.NS_BF16, "fp32": nsg.NS_FP32_GRAM, "fp32gs": nsg.NS_FP32_GRAM_SPACE}[args.gram]
+    mode = {"bf16": nsg.NS_BF16, "fp32": nsg.NS_FP32_GRAM, "fp32gs": nsg.NS_FP32_GRAM_SPACE,
+            "fp32auto": nsg.NS_FP32_AUTO}[args.gram]
     stream = torch.cuda.current_stream(dev)
     results, tot_ms, tot_mats, tot_flops = [], 0.0, 0, 0
     runs = [(f"{m}x{a * m}", [(m, a * m)] * bt, 5000 + m + a) for (m, a, bt) in pts]

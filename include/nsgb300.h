@@ -55,7 +55,12 @@ enum {
    * per step Q = aI + bA + cA^2, A <- Q A Q, P <- Q P on m x m matrices only,
    * and X_k = P X_0 at the end. Exact reformulation of the same iteration;
    * fewer flops when n is well above m. bf16 in, fp32 out. */
-  NS_FP32_GRAM_SPACE = 2
+  NS_FP32_GRAM_SPACE = 2,
+  /* Per shape bucket, Gram-space when n >= 2m and NS_FP32_GRAM otherwise:
+   * with k = 5 steps Gram-space does 4m^2n + 8km^3 flops against the
+   * standard k(4m^2n + 2m^3), fewer once n > 1.875 m. Same precision and
+   * results per matrix as the mode chosen for its bucket. bf16 in, fp32 out. */
+  NS_FP32_AUTO = 3
 };
 
 /* Data model of a plan. */

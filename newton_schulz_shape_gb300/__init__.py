@@ -16,7 +16,7 @@ import ctypes
 
 from ._lib import (NS_BF16, NS_ERR_ARG, NS_ERR_CUDA, NS_ERR_DEVICE_CHECK, NS_ERR_HOME,  # noqa: F401
                    NS_ERR_NOT_DIVISIBLE, NS_ERR_SHAPE, NS_ERR_TIMEOUT, NS_ERR_UNSUPPORTED,
-                   NS_ERR_WORKSPACE, NS_FP32_GRAM, NS_FP32_GRAM_SPACE, NS_LAYOUT_FLAT, NS_LAYOUT_ROW_SHARD, NS_LAYOUT_TWO_STAGE, NS_OK,
+                   NS_ERR_WORKSPACE, NS_FP32_GRAM, NS_FP32_GRAM_SPACE, NS_FP32_AUTO, NS_LAYOUT_FLAT, NS_LAYOUT_ROW_SHARD, NS_LAYOUT_TWO_STAGE, NS_OK,
                    LIB_PATH, NsError, check, header_symbols, i32_array, i64_array, lib, ptr_array)
 
 A_COEF, B_COEF, C_COEF = 3.4445, -4.7750, 2.0315

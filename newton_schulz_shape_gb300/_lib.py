@@ -28,6 +28,7 @@ NS_ERR_WORKSPACE = -9
 NS_BF16 = 0
 NS_FP32_GRAM = 1
 NS_FP32_GRAM_SPACE = 2
+NS_FP32_AUTO = 3
 NS_LAYOUT_ROW_SHARD = 0
 NS_LAYOUT_FLAT = 1
 NS_LAYOUT_TWO_STAGE = 2

@@ -1044,6 +1044,15 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
   char* ws = static_cast<char*>(workspace);
   if (p.gram_mode == NS_FP32_GRAM) return orthogonalize_f32(p, in, out, ws, nsm, status, st);
   if (p.gram_mode == NS_FP32_GRAM_SPACE) return orthogonalize_gram_space(p, in, out, ws, nsm, status, st);
+  if (p.gram_mode == NS_FP32_AUTO) {
+    // per bucket: standard fp32-Gram iteration or Gram space, one workspace
+    if (!plan->view_std.buckets.empty()) {
+      rc = orthogonalize_f32(plan->view_std, in, out, ws, nsm, status, st);
+      if (rc != NS_OK) return rc;
+    }
+    if (!plan->view_gs.buckets.empty()) return orthogonalize_gram_space(plan->view_gs, in, out, ws, nsm, status, st);
+    return NS_OK;
+  }
 
   rc = prologue_bf16(p, in, out, ws, status, st);
   if (rc != NS_OK) return rc;

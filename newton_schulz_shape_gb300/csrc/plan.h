@@ -42,6 +42,7 @@ struct Bucket {
   uint64_t off_scale = 0;    // float scale per member
   uint64_t off_coef = 0;     // fp32 Gram-space: 3 floats per member (Q coefficients)
   int64_t nchunks = 0;       // sum-of-squares chunks per matrix
+  bool gram_space = false;   // fp32: run this bucket in Gram space (NS_FP32_GRAM_SPACE, or NS_FP32_AUTO with n >= 2m)
 };
 
 struct Plan {
@@ -79,4 +80,7 @@ int build_subplan(const Plan& base, const std::vector<int>& members, Plan& out);
 // The opaque handle behind ns_plan_t.
 struct ns_plan {
   nsplan::Plan p;
+  // NS_FP32_AUTO: the plan's standard-fp32 and Gram-space buckets as two
+  // views (same tensors, ordinals and workspace offsets), built at creation
+  nsplan::Plan view_std, view_gs;
 };

@@ -119,7 +119,8 @@ int finish(Plan& p, bool keep_homes = false) {
   // fp32 Gram-space path: one X set, then (hi, lo) pairs of T, P0, P1 in the
   // second X region.
   const bool f32 = p.gram_mode != NS_BF16;
-  const bool gs = p.gram_mode == NS_FP32_GRAM_SPACE;
+  const bool gs_all = p.gram_mode == NS_FP32_GRAM_SPACE;
+  const bool gs_auto = p.gram_mode == NS_FP32_AUTO;
   const uint64_t xset = f32 ? 4 * 4 : 2;
   const uint64_t aset = f32 ? 2 * 4 : 2;
   uint64_t off = 0;
@@ -136,6 +137,8 @@ int finish(Plan& p, bool keep_homes = false) {
       p.t[b.members[s]].bucket = static_cast<int>(bi);
       p.t[b.members[s]].slot = static_cast<int>(s);
     }
+    b.gram_space = gs_all || (gs_auto && b.n >= 2 * b.m);
+    const bool gs = b.gram_space;
     const uint64_t xbytes = cnt * uint64_t(b.m_pad) * uint64_t(b.n_pad) * xset;
     const uint64_t abytes = cnt * uint64_t(b.m_pad) * uint64_t(b.m_pad) * aset;
     b.off_x0 = take(xbytes);
@@ -464,10 +467,27 @@ namespace {
 int check_coeffs(int steps, float eps, int gram_mode, float ridge) {
   if (steps < 0) return NS_ERR_ARG;
   if (!(eps >= 0.0f)) return NS_ERR_ARG;
-  if (gram_mode != NS_BF16 && gram_mode != NS_FP32_GRAM && gram_mode != NS_FP32_GRAM_SPACE) return NS_ERR_ARG;
+  if (gram_mode != NS_BF16 && gram_mode != NS_FP32_GRAM && gram_mode != NS_FP32_GRAM_SPACE &&
+      gram_mode != NS_FP32_AUTO)
+    return NS_ERR_ARG;
   if (!(ridge >= 0.0f)) return NS_ERR_ARG;
   if (gram_mode == NS_BF16 && ridge != 0.0f) return NS_ERR_ARG;
   return NS_OK;
+}
+// NS_FP32_AUTO: split the plan's buckets into the standard-fp32 and the
+// Gram-space view. Each view keeps every tensor (ordinals index the caller's
+// pointer arrays) and the buckets' workspace offsets.
+void make_mode_views(ns_plan* pl) {
+  if (pl->p.gram_mode != NS_FP32_AUTO) return;
+  pl->view_std = pl->p;
+  pl->view_gs = pl->p;
+  pl->view_std.buckets.clear();
+  pl->view_gs.buckets.clear();
+  for (const nsplan::Bucket& b : pl->p.buckets) (b.gram_space ? pl->view_gs : pl->view_std).buckets.push_back(b);
+  for (nsplan::Plan* v : {&pl->view_std, &pl->view_gs}) {
+    v->route.clear();  // views never route
+    for (int d = 0; d < nsplan::kMaxDevices; ++d) v->d_route[d] = nullptr;
+  }
 }
 }  // namespace
 
@@ -508,6 +528,7 @@ int ns_plan_create(int n_tensors, const int32_t* ndims, const int64_t* shapes_fl
     delete pl;
     return rc;
   }
+  make_mode_views(pl);
   *plan_out = pl;
   return NS_OK;
 }
@@ -536,6 +557,7 @@ int ns_plan_create_two_stage(int n_tensors, const int32_t* ndims, const int64_t*
     delete pl;
     return rc;
   }
+  make_mode_views(pl);
   *plan_out = pl;
   return NS_OK;
 }
@@ -565,6 +587,7 @@ int ns_plan_create_flat(int n_tensors, const int32_t* ndims, const int64_t* shap
     delete pl;
     return rc;
   }
+  make_mode_views(pl);
   *plan_out = pl;
   return NS_OK;
 }

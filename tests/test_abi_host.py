@@ -216,6 +216,24 @@ def test_workspace_bytes_layout():
     assert nsg.ns_plan_create([], S=1).workspace_bytes() == 0
 
 
+def test_fp32_auto_workspace_follows_each_bucket_mode():
+    # a bucket with n >= 2m takes the Gram-space layout, others the standard
+    # fp32 layout: single-bucket auto plans equal the plan of that mode
+    for shape, mode in [((256, 1024), nsg.NS_FP32_GRAM_SPACE), ((1024, 256), nsg.NS_FP32_GRAM_SPACE),
+                        ((300, 500), nsg.NS_FP32_GRAM), ((512, 512), nsg.NS_FP32_GRAM)]:
+        auto = nsg.ns_plan_create([shape], gram_mode=nsg.NS_FP32_AUTO, S=1)
+        pure = nsg.ns_plan_create([shape], gram_mode=mode, S=1)
+        assert auto.workspace_bytes() == pure.workspace_bytes(), shape
+        assert auto.gram_mode == nsg.NS_FP32_AUTO and auto.out_bytes == 4
+    mixed = nsg.ns_plan_create([(256, 1024), (512, 512)], gram_mode=nsg.NS_FP32_AUTO, S=1)
+    parts = [nsg.ns_plan_create([s], gram_mode=m, S=1).workspace_bytes()
+             for s, m in [((256, 1024), nsg.NS_FP32_GRAM_SPACE), ((512, 512), nsg.NS_FP32_GRAM)]]
+    assert mixed.workspace_bytes() == sum(parts)
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_plan_create([(4, 4)], gram_mode=4, S=1)
+    assert e.value.code == nsg.NS_ERR_ARG
+
+
 @pytest.mark.parametrize("R,T", [(1, 1), (2, 2), (4, 2), (2, 4)])
 def test_two_stage_plan_vs_oracle(R, T):
     shapes = [(32, 16), (16, 32, 2), (64, 8), (8, 8, 8), (16, 24)]

@@ -148,3 +148,21 @@ def test_gram_space_agrees_with_fp32_gram_path():
     for t, x, y in zip(ts, a, b):
         assert rel_err(x, y.cpu().numpy()) <= FP32_TOL
         assert rel_err(x, oracle(t)) <= FP32_TOL
+
+
+# NS_FP32_AUTO: per shape bucket, Gram space when n >= 2m, else the standard
+# fp32-Gram iteration. Each matrix must come out bit for bit as in the plan of
+# the mode its bucket was given, and within the fp32 bar of the oracle.
+AUTO_SHAPES = [(256, 1024), (1024, 256), (300, 300), (200, 350), (128, 2048), (130, 130)]
+
+
+def test_fp32_auto_matches_the_mode_of_each_bucket():
+    ts = workloads.gen_tensors(workloads.Workload("auto", AUTO_SHAPES, 0.02, 85))
+    auto = run_mode(AUTO_SHAPES, ts, nsg.NS_FP32_AUTO)
+    for s, t, o in zip(AUTO_SHAPES, ts, auto):
+        r, c = s[0], s[1]
+        m, n = min(r, c), max(r, c)
+        mode = nsg.NS_FP32_GRAM_SPACE if n >= 2 * m else nsg.NS_FP32_GRAM
+        alone = run_mode([s], [t], mode)[0]
+        assert torch.equal(o.cpu(), alone.cpu()), s
+        assert rel_err(o, oracle(t)) <= FP32_TOL, s
