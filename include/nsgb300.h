@@ -223,7 +223,10 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
  * on three streams owned by the pipeline: the pack and prologue of a wave
  * overlap the NS products of the previous wave, and the unpack of a wave
  * overlaps the next one. Buffers as in ns_pack_to_home / ns_unpack_from_home
- * (home_in receives the gathered inputs, home_out the results). workspace
+ * (home_in receives the gathered inputs, home_out the results); for row-shard
+ * plans with shard_dim 0 the prologue reads the rank buffers directly, every
+ * row of a tensor being contiguous in one of them, and home_in is left
+ * untouched. workspace
  * holds two wave workspaces (ns_pipeline_info), 256-byte aligned. The call
  * is ordered after prior work on `stream`, and later work on `stream` waits
  * for all of it. The first run on a device creates the pipeline's streams

@@ -875,8 +875,11 @@ int orthogonalize_f32(const Plan& p, const void* const* in, void* const* out, ch
 
 // bf16 path, part 1: sums of squares, scales, X_0 = scale * (T or T^T),
 // zero padded into the workspace.
+// With rank_in (row-shard plans, shard_dim 0) the rows are read straight from
+// the S rank buffers, which fuses the pack to the home buffers away; `in` is
+// then unused.
 int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* ws, unsigned int* status,
-                  cudaStream_t st) {
+                  cudaStream_t st, const void* const* rank_in = nullptr) {
   // prologue: X~_0 = T or T^T (unscaled, zero padded) with per-stripe sums of
   // squares in one pass, then the scales
   for (const Bucket& b : p.buckets) {
@@ -894,11 +897,21 @@ int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* 
       pp.eps = p.eps;
       pp.out_f32 = 0;
       pp.status = status;
+      if (rank_in) {
+        pp.from_ranks = 1;
+        pp.ranks_aligned = 1;
+        for (int r = 0; r < p.S; ++r) {
+          pp.rank_ptr[r] = rank_in[r];
+          if (reinterpret_cast<uintptr_t>(rank_in[r]) & 15) pp.ranks_aligned = 0;
+        }
+      }
       for (int k = 0; k < pp.count; ++k) {
         const size_t s = s0 + k;
         const Tensor& t = p.t[b.members[s]];
         nsk::MatDesc& d = pp.md[k];
-        d.in = in[t.ordinal];
+        d.in = rank_in ? nullptr : in[t.ordinal];
+        d.rank_off = t.rank_off;
+        d.shard_rows = static_cast<int>(t.rows / p.S);
         d.out = out[t.ordinal];
         d.x = q.x0 + s * b.m_pad * b.n_pad * 2;
         d.partial = q.partial + s * b.nchunks;
@@ -1204,6 +1217,10 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaEvent_t* ev = pd.ev.data();
   const int sd = p.layout == NS_LAYOUT_ROW_SHARD ? p.shard_dim : 0;
+  // row shards along dim 0: every row of a tensor is contiguous in one rank
+  // buffer, so the prologue reads the rank buffers and the pack to home_in is
+  // skipped
+  const bool fused_pack = p.layout == NS_LAYOUT_ROW_SHARD && p.shard_dim == 0;
   if (cudaEventRecord(ev[0], st) != cudaSuccess || cudaStreamWaitEvent(pd.mem, ev[0], 0) != cudaSuccess ||
       cudaStreamWaitEvent(pd.gemm, ev[0], 0) != cudaSuccess || cudaStreamWaitEvent(pd.out, ev[0], 0) != cudaSuccess)
     return NS_ERR_CUDA;
@@ -1214,9 +1231,11 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
     char* ws = static_cast<char*>(workspace) + (w % 2) * pl->ws_half;
     cudaEvent_t ev_pro = ev[4 + 2 * w], ev_gemm = ev[5 + 2 * w];
     if (w >= 2 && cudaStreamWaitEvent(pd.mem, ev[5 + 2 * (w - 2)], 0) != cudaSuccess) return NS_ERR_CUDA;
-    rc = route(pl->base, const_cast<void* const*>(rank_in), home_in, S, sd, true, p.in_bytes, pd.mem,
-               pl->g_begin[w], pl->g_end[w]);
-    if (rc != NS_OK) return rc;
+    if (!fused_pack) {
+      rc = route(pl->base, const_cast<void* const*>(rank_in), home_in, S, sd, true, p.in_bytes, pd.mem,
+                 pl->g_begin[w], pl->g_end[w]);
+      if (rc != NS_OK) return rc;
+    }
     ins.assign(wp.part.size(), nullptr);
     outs.assign(wp.part.size(), nullptr);
     for (size_t j = 0; j < wp.part.size(); ++j) {
@@ -1225,7 +1244,7 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
       outs[j] = static_cast<char*>(home_out[t.home]) + t.home_off * p.out_bytes;
     }
     if (!wp.buckets.empty()) {
-      rc = prologue_bf16(wp, ins.data(), outs.data(), ws, status, pd.mem);
+      rc = prologue_bf16(wp, ins.data(), outs.data(), ws, status, pd.mem, fused_pack ? rank_in : nullptr);
       if (rc != NS_OK) return rc;
     }
     if (cudaEventRecord(ev_pro, pd.mem) != cudaSuccess || cudaStreamWaitEvent(pd.gemm, ev_pro, 0) != cudaSuccess)

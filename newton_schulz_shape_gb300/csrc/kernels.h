@@ -119,6 +119,7 @@ struct Ridge32Params {
 
 // ------------------------------------------------------- prologue / store
 constexpr int PRO_MAX_MATS = 192;
+constexpr int ROUTE_MAX_RANKS = 64;
 
 struct MatDesc {
   const void* in;       // original tensor, row-major (rows x cols), bf16
@@ -131,6 +132,10 @@ struct MatDesc {
   long long numel;
   int rows, cols;
   int transposed;
+  long long rank_off;   // rank-buffer input (ProParams.from_ranks): element offset of this tensor's
+                        // shard in every rank buffer; row j of the tensor is row j % shard_rows of
+                        // the shard on rank j / shard_rows
+  int shard_rows;
 };
 
 struct ProParams {
@@ -143,11 +148,14 @@ struct ProParams {
   int out_f32;          // result dtype: 0 bf16, 1 fp32
   long long x_split;    // fp32-Gram: elements between the X hi / X lo / X^T hi / X^T lo buffers
   int apply_scale;      // store: multiply by *scale (bf16 path with zero steps)
+  int from_ranks;       // bf16 prep: read the tensors' rows from the rank buffers (row shards along
+                        // dim 0) instead of md[].in: the pack to the home buffer is fused away
+  int ranks_aligned;    // every rank_ptr is 16-byte aligned
+  const void* rank_ptr[ROUTE_MAX_RANKS];
   unsigned int* status;
 };
 
 // ----------------------------------------------------------- pack / unpack
-constexpr int ROUTE_MAX_RANKS = 64;
 
 struct RouteEntry {
   long long seg_begin;  // first position of the tensor in the rank coordinate space

@@ -123,11 +123,21 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
   const MatDesc& d = p.md[blockIdx.y];
   const unsigned short* __restrict__ src = reinterpret_cast<const unsigned short*>(d.in);
   uint4* __restrict__ x4 = reinterpret_cast<uint4*>(d.x);
+  // row j of the input tensor (d.cols elements): contiguous in its home
+  // buffer, or in the rank buffer holding its row shard
+  const long long row_len = d.cols;
+  auto trow = [&](long long j) -> const unsigned short* {
+    if (!p.from_ranks) return src + j * row_len;
+    const int r = static_cast<int>(j / d.shard_rows);
+    return reinterpret_cast<const unsigned short*>(p.rank_ptr[r]) + d.rank_off + (j - static_cast<long long>(r) * d.shard_rows) * row_len;
+  };
+  const bool base_aligned = p.from_ranks ? (p.ranks_aligned && d.rank_off % 8 == 0)
+                                         : (reinterpret_cast<uintptr_t>(src) & 15) == 0;
   const int nv = p.n_pad / 8;  // 16-byte vectors per X~_0 row
   const int i0 = blockIdx.x * TILE;
   float acc = 0.0f;
   if (!d.transposed) {
-    const bool vec = (p.n % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+    const bool vec = (p.n % 8 == 0) && base_aligned;
     const int total = TILE * nv;
     constexpr int U = 4;
     for (int base = threadIdx.x; base < total; base += U * PREP_THREADS) {
@@ -138,12 +148,13 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
         const int i = i0 + v / nv, j0 = (v % nv) * 8;
         q[u] = make_uint4(0, 0, 0, 0);
         if (v < total && i < p.m) {
+          const unsigned short* row = trow(i);
           if (vec && j0 + 8 <= p.n) {
-            q[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(i) * p.n + j0));
+            q[u] = __ldg(reinterpret_cast<const uint4*>(row + j0));
           } else if (j0 < p.n) {
             uint16_t h[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = j0 + k < p.n ? src[static_cast<long long>(i) * p.n + j0 + k] : 0;
+            for (int k = 0; k < 8; ++k) h[k] = j0 + k < p.n ? row[j0 + k] : 0;
             q[u] = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
                               h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
           }
@@ -161,7 +172,7 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
   } else {
     // X~[i][j] = T[j][i], T row-major n x m (rows j, cols i)
     __shared__ uint32_t tile[2][TILE][TILE / 2 + 1];
-    const bool vec = (p.m % 8 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
+    const bool vec = (p.m % 8 == 0) && base_aligned;
     const int ntiles = p.n_pad / TILE;
     // each thread moves two 16-byte vectors per tile: vector q = threadIdx.x + 256 h
     auto load = [&](int jt, uint4 (&r)[2]) {
@@ -171,12 +182,13 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
         const int j = jt * TILE + q / 8, i = i0 + (q % 8) * 8;
         r[h] = make_uint4(0, 0, 0, 0);
         if (j < p.n && i < p.m) {
+          const unsigned short* row = trow(j);
           if (vec && i + 8 <= p.m) {
-            r[h] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(j) * p.m + i));
+            r[h] = __ldg(reinterpret_cast<const uint4*>(row + i));
           } else {
             uint16_t e[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) e[k] = i + k < p.m ? src[static_cast<long long>(j) * p.m + i + k] : 0;
+            for (int k = 0; k < 8; ++k) e[k] = i + k < p.m ? row[i + k] : 0;
             r[h] = make_uint4(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16),
                               e[4] | (uint32_t(e[5]) << 16), e[6] | (uint32_t(e[7]) << 16));
           }
