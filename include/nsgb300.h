@@ -224,9 +224,11 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
  * overlap the NS products of the previous wave, and the unpack of a wave
  * overlaps the next one. Buffers as in ns_pack_to_home / ns_unpack_from_home
  * (home_in receives the gathered inputs, home_out the results); for row-shard
- * plans with shard_dim 0 the prologue reads the rank buffers directly, every
- * row of a tensor being contiguous in one of them, and home_in is left
- * untouched. workspace
+ * plans with shard_dim 0, where every row of a tensor is contiguous in one
+ * rank buffer, the prologue reads the rank buffers directly and the last B*X
+ * launch of each wave writes the results straight into rank_out, so home_in
+ * and home_out are left untouched (a wave whose last launch cannot address
+ * all its matrices still stages its results in home_out). workspace
  * holds two wave workspaces (ns_pipeline_info), 256-byte aligned. The call
  * is ordered after prior work on `stream`, and later work on `stream` waits
  * for all of it. The first run on a device creates the pipeline's streams

@@ -211,7 +211,8 @@ BucketPtrs bucket_ptrs(const Bucket& b, char* ws) {
 // entry is the output address with bit 0 set for transposed tensors.
 template <typename P>
 int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1,
-               unsigned int* status, void* const* final_out, int cl, bool first_step) {
+               unsigned int* status, void* const* final_out, int cl, bool first_step,
+               void* const* final_ranks = nullptr) {
   std::memset(&gp, 0, sizeof(gp));
   gp.alpha = p.a;
   gp.beta = p.b;
@@ -279,7 +280,10 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
         g.out_first = n_out;
         for (size_t s = 0; s < cnt; ++s) {
           const Tensor& t = p.t[b.members[s]];
-          const unsigned long long a = reinterpret_cast<unsigned long long>(final_out[t.ordinal]);
+          // the tensor's output address, or (row shards along dim 0) its
+          // shard offset in every rank buffer
+          const unsigned long long a = final_ranks ? static_cast<unsigned long long>(t.rank_off) << 1
+                                                   : reinterpret_cast<unsigned long long>(final_out[t.ordinal]);
           gp.out_tab[n_out++] = a | (t.transposed ? 1ull : 0ull);
         }
       }
@@ -289,6 +293,11 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
   }
   gp.nb = nb;
   gp.total_tiles = tiles;
+  if (final_ranks) {
+    gp.out_ranks = 1;
+    gp.S = p.S;
+    for (int r = 0; r < p.S; ++r) gp.rank_ptr[r] = final_ranks[r];
+  }
   return NS_OK;
 }
 
@@ -306,12 +315,13 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
              : NS_ERR_CUDA;
 }
 
-// B*X phase of the last step, storing results directly into `out`.
+// B*X phase of the last step, storing results directly into `out`, or with
+// rank_out (row shards along dim 0) into the S rank buffers.
 int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
-                 void* const* out, bool first_step, bool reverse, cudaStream_t st) {
-  static thread_local nsk::GemmFinalParams gp;  // ~31 KB: kept off the stack
+                 void* const* out, bool first_step, bool reverse, cudaStream_t st, void* const* rank_out = nullptr) {
+  static thread_local nsk::GemmFinalParams gp;  // ~32 KB: kept off the stack
   const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
-  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step);
+  int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step, rank_out);
   gp.reverse = reverse ? 1 : 0;
   if (rc != NS_OK) return rc;
   return counted(nsk::PH_BX, st, [&] {
@@ -929,8 +939,22 @@ int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* 
   return NS_OK;
 }
 
+// Whether every bucket group's last B*X launch can store its results itself
+// (its per-matrix table fits the parameter block) and there is a last step.
+bool final_stores_all(const Plan& p) {
+  if (p.steps == 0) return false;
+  for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS)
+    if (group_matrices(p, b0, std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS)) > size_t(nsk::GEMM_MAX_OUT))
+      return false;
+  return true;
+}
+
 // bf16 path, part 2: k steps of (Gram, A*A + B, B*X) and the final store.
-int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int* status, cudaStream_t st) {
+// With rank_out (row shards along dim 0, final_stores_all(p)) the results go
+// straight to the S rank buffers, fusing the unpack away; `out` is then unused.
+int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int* status, cudaStream_t st,
+               void* const* rank_out = nullptr) {
+  if (rank_out && !final_stores_all(p)) return NS_ERR_ARG;
   int rc = NS_OK;
   // k steps x (Gram, A*A + B, B*X) over all buckets. The last B*X launch of
   // a bucket group writes the results straight to `out` when its per-matrix
@@ -946,7 +970,7 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
         // starting on the matrices the previous product wrote last (still in L2)
         const bool serp = ((step * 3 + phase) & 1) != 0;
         if (last && phase == nsk::PH_BX && group_matrices(p, b0, b1) <= size_t(nsk::GEMM_MAX_OUT)) {
-          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, serp, st);
+          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, serp, st, rank_out);
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
           rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, serp, st);
@@ -1249,15 +1273,20 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
     }
     if (cudaEventRecord(ev_pro, pd.mem) != cudaSuccess || cudaStreamWaitEvent(pd.gemm, ev_pro, 0) != cudaSuccess)
       return NS_ERR_CUDA;
+    // the last B*X launches write the rank buffers themselves when the pack
+    // was fused and every launch can store its results
+    const bool fused_unpack = fused_pack && !wp.buckets.empty() && final_stores_all(wp);
     if (!wp.buckets.empty()) {
-      rc = steps_bf16(wp, outs.data(), ws, nsm, status, pd.gemm);
+      rc = steps_bf16(wp, outs.data(), ws, nsm, status, pd.gemm, fused_unpack ? rank_out : nullptr);
       if (rc != NS_OK) return rc;
     }
     if (cudaEventRecord(ev_gemm, pd.gemm) != cudaSuccess || cudaStreamWaitEvent(pd.out, ev_gemm, 0) != cudaSuccess)
       return NS_ERR_CUDA;
-    rc = route(pl->base, rank_out, const_cast<void* const*>(home_out), S, sd, false, p.out_bytes, pd.out,
-               pl->g_begin[w], pl->g_end[w]);
-    if (rc != NS_OK) return rc;
+    if (!fused_unpack) {
+      rc = route(pl->base, rank_out, const_cast<void* const*>(home_out), S, sd, false, p.out_bytes, pd.out,
+                 pl->g_begin[w], pl->g_end[w]);
+      if (rc != NS_OK) return rc;
+    }
   }
   if (cudaEventRecord(ev[1], pd.mem) != cudaSuccess || cudaEventRecord(ev[2], pd.gemm) != cudaSuccess ||
       cudaEventRecord(ev[3], pd.out) != cudaSuccess || cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess ||

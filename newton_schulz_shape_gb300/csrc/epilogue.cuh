@@ -208,24 +208,58 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
         // row r of X_k (m index), columns cg.. (n index) -> the caller's tensor
         if (r < B.m_valid) {
           const unsigned long long en = p.out_tab[B.out_first + e.mat];
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(en & ~1ull);
-          if (!(en & 1ull)) {
-            __nv_bfloat16* dst = o + static_cast<long long>(r) * B.n_valid + cg;
-            if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
+          if (!p.out_ranks) {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(en & ~1ull);
+            if (!(en & 1ull)) {
+              __nv_bfloat16* dst = o + static_cast<long long>(r) * B.n_valid + cg;
+              if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) d4[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                for (int u = 0; u < 4; ++u) d4[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.n_valid) dst[j] = hv[j];
+              }
             } else {
+              // transposed tensor: element (r, c) of X_k is element (c, r) of
+              // the output; lanes hold consecutive r, so each store is contiguous
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (cg + j < B.n_valid) dst[j] = hv[j];
+                if (cg + j < B.n_valid) o[static_cast<long long>(cg + j) * B.m_valid + r] = hv[j];
             }
           } else {
-            // transposed tensor: element (r, c) of X_k is element (c, r) of
-            // the output; lanes hold consecutive r, so each store is contiguous
+            // row shards along dim 0: row j of the output tensor is row
+            // j % sh of the shard at offset en >> 1 of rank buffer j / sh
+            const long long off = static_cast<long long>(en >> 1);
+            if (!(en & 1ull)) {
+              const int sh = B.m_valid / p.S;
+              const int rk = r / sh;
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.rank_ptr[rk]) + off +
+                                   static_cast<long long>(r - rk * sh) * B.n_valid + cg;
+              if (cg + 32 <= B.n_valid && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (cg + j < B.n_valid) o[static_cast<long long>(cg + j) * B.m_valid + r] = hv[j];
+                for (int u = 0; u < 4; ++u) d4[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.n_valid) dst[j] = hv[j];
+              }
+            } else {
+              // transposed: output rows cg .. cg + 31, walked without dividing
+              const int sh = B.n_valid / p.S;
+              int rk = cg / sh, lr = cg - rk * sh;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (cg + j < B.n_valid)
+                  reinterpret_cast<__nv_bfloat16*>(p.rank_ptr[rk])[off + static_cast<long long>(lr) * B.m_valid + r] = hv[j];
+                if (++lr == sh) {
+                  ++rk;
+                  lr = 0;
+                }
+              }
+            }
           }
         }
         // every lane's slot reads are done before the slot is reloaded

@@ -12,6 +12,7 @@ namespace nsk {
 
 // ------------------------------------------------------------------- GEMMs
 constexpr int GEMM_MAX_BUCKETS = 8;
+constexpr int ROUTE_MAX_RANKS = 64;
 enum GemmPhase { PH_GRAM = 0, PH_A2B = 1, PH_BX = 2 };
 
 struct GemmBucket {
@@ -35,8 +36,11 @@ struct GemmBucket {
 
 // Final-store launches of the B*X phase write each result straight to the
 // caller's output tensor; out_tab holds one entry per matrix: the output
-// address with bit 0 set when the tensor was transposed (rows > cols).
-constexpr int GEMM_MAX_OUT = 3520;
+// address with bit 0 set when the tensor was transposed (rows > cols). With
+// out_ranks the results go straight to the S rank buffers instead (row
+// shards along dim 0): the entry is the tensor's shard offset in every rank
+// buffer (elements) shifted left by one, with the same bit 0.
+constexpr int GEMM_MAX_OUT = 3440;
 
 template <int NOUT>
 struct GemmParamsT {
@@ -51,6 +55,9 @@ struct GemmParamsT {
   int nb;
   float alpha, beta, gamma;  // a, b, c of the quintic step
   int reverse;               // walk the tiles last to first (serpentine order across launches)
+  int out_ranks;             // final-store launches: out_tab holds rank-buffer offsets
+  int S;                     // ranks of rank_ptr (out_ranks)
+  void* rank_ptr[ROUTE_MAX_RANKS];
   unsigned int* status;
   unsigned long long out_tab[NOUT];
 };
@@ -119,7 +126,6 @@ struct Ridge32Params {
 
 // ------------------------------------------------------- prologue / store
 constexpr int PRO_MAX_MATS = 192;
-constexpr int ROUTE_MAX_RANKS = 64;
 
 struct MatDesc {
   const void* in;       // original tensor, row-major (rows x cols), bf16

@@ -170,15 +170,22 @@ def test_wave_pipeline_equals_serial_step(n_waves):
     for _ in range(2):   # run twice: the second run reuses streams, events and workspaces
         nsg.ns_pipeline_run(pipe, rank_in, hi2, ho2, ro2, pws)
     assert nsg.ns_check_status(plan) == nsg.NS_OK
-    for a, b in zip(ho1, ho2):
-        assert torch.equal(a, b)
+    # row shards along dim 0: the pipeline reads the rank buffers and its last
+    # B*X launches write them, so the home buffers stay untouched
+    for a in hi2 + ho2:
+        assert not a.any()
     for a, b in zip(ro1, ro2):
         assert torch.equal(a, b)
-    # and the serial result itself is right (sampled)
+    # and the result itself is right (sampled): tensor i rebuilt from its row
+    # shards in the output rank buffers
+    from gpu_util import BF16_TOL, oracle_ns, rel_err
+    offs = [0]
+    for t in ts:
+        offs.append(offs[-1] + t.numel() // S)
     for i in (0, 3, len(shapes) - 1):
-        y = ho2[homes[i]][ho[i]:ho[i] + ts[i].numel()].reshape(ts[i].shape)
-        from gpu_util import BF16_TOL, oracle_ns, rel_err
+        y = torch.cat([ro2[r][offs[i]:offs[i + 1]] for r in range(S)]).reshape(ts[i].shape)
         assert rel_err(y, oracle_ns(ts[i])) <= BF16_TOL
+        assert torch.equal(y, ho1[homes[i]][ho[i]:ho[i] + ts[i].numel()].reshape(ts[i].shape))
 
 
 def _e2e_check(plan, shapes, ts, rank_in, S, participating, pipe_waves=0):
