@@ -268,7 +268,9 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * Not part of the pages' interface: support for measuring the kernels above.
  * Kernel kinds: 0 = Gram (X X^T), 1 = A*A with the b*A + c*A^2 epilogue,
  * 2 = B*X with the a*X epilogue, 3 = norm/scale/transpose prologue and
- * output store, 4 = pack/unpack. Launch counters are always on. When timing
+ * output store, 4 = pack/unpack, 5 = the last step's B*X launches, which also
+ * store the results (to the caller's tensors or the rank buffers). Launch
+ * counters are always on. When timing
  * is enabled, every launch is bracketed by two CUDA events recorded on the
  * stream it is launched on; ns_profile_read synchronises those events. */
 
@@ -286,7 +288,7 @@ int ns_set_gemm_cluster(int cl);
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */
 int ns_profile_enable(int enable);
 
-/* launches[5] (may be NULL) receives the launch count per kind and gpu_ms[5]
+/* launches[6] (may be NULL) receives the launch count per kind and gpu_ms[6]
  * (may be NULL) the summed event time per kind since the last reset; reset
  * != 0 clears both afterwards. */
 int ns_profile_read(int reset, int64_t* launches, double* gpu_ms);

@@ -231,7 +231,7 @@ def ns_check_status(plan: NsPlan = None, stream=None) -> int:
     return lib.ns_check_status(plan.handle if plan is not None else None, _stream(stream))
 
 
-KERNEL_KINDS = ("gram", "a2b", "bx", "prologue_store", "pack_unpack")
+KERNEL_KINDS = ("gram", "a2b", "bx", "prologue_store", "pack_unpack", "bx_final")
 
 
 def ns_profile_enable(enable: bool = True) -> None:
@@ -241,8 +241,8 @@ def ns_profile_enable(enable: bool = True) -> None:
 
 def ns_profile_read(reset: bool = False):
     """Return ({kind: launches}, {kind: summed gpu ms}) since the last reset."""
-    n = (ctypes.c_int64 * 5)()
-    ms = (ctypes.c_double * 5)()
+    n = (ctypes.c_int64 * len(KERNEL_KINDS))()
+    ms = (ctypes.c_double * len(KERNEL_KINDS))()
     check(lib.ns_profile_read(1 if reset else 0, n, ms), "ns_profile_read")
     return dict(zip(KERNEL_KINDS, list(n))), dict(zip(KERNEL_KINDS, list(ms)))
 

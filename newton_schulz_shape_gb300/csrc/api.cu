@@ -43,8 +43,8 @@ EncodeTiledFn g_encode = nullptr;
 int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
 
 // ----------------------------------------------------------- measurement
-constexpr int kKinds = 5;
-enum { K_GRAM = 0, K_A2B = 1, K_BX = 2, K_PRO = 3, K_PACK = 4 };
+constexpr int kKinds = 6;
+enum { K_GRAM = 0, K_A2B = 1, K_BX = 2, K_PRO = 3, K_PACK = 4, K_BX_FINAL = 5 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 long long g_launches[kKinds] = {0};
@@ -324,7 +324,7 @@ int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, 
   int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step, rank_out);
   gp.reverse = reverse ? 1 : 0;
   if (rc != NS_OK) return rc;
-  return counted(nsk::PH_BX, st, [&] {
+  return counted(K_BX_FINAL, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(cl, gp, nsm, st);
          }) == cudaSuccess
              ? NS_OK
@@ -751,7 +751,7 @@ int orthogonalize_gram_space(const Plan& p, const void* const* in, void* const* 
         if (rc != NS_OK) return rc;
       }
       const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-      if (counted(K_BX, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
+      if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
         return NS_ERR_CUDA;
     } else {
       return NS_ERR_UNSUPPORTED;  // more matrices than one final launch can address
@@ -817,7 +817,7 @@ int orthogonalize_f32(const Plan& p, const void* const* in, void* const* out, ch
           rc = fill_phase32(gp, p, ws, phase, cur, b0, b1, status, out);
           if (rc != NS_OK) return rc;
           const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-          if (counted(K_BX, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
+          if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
             return NS_ERR_CUDA;
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
