@@ -272,3 +272,60 @@ def test_two_stage_model_pack_ns_unpack(waves):
     full = orr.route_two_stage_back([bits(h) for h in home_out], shapes, pd, dict(enumerate(homes)), R, T)
     for r in range(R * T):
         assert np.array_equal(bits(rank_out[r]), full[r][:rank_out[r].numel()])
+
+
+def _pipeline_vs_serial(shapes, S, shard_dim, n_waves, seed):
+    """Run pack -> NS -> unpack as three serial calls and through the wave
+    pipeline; the rank outputs must agree bit for bit. Returns both results."""
+    dev = torch.device("cuda:0")
+    ts = workloads.gen_tensors(workloads.Workload("pipe", shapes, 0.02, seed))
+    plan = nsg.ns_plan_create(shapes, S=S, shard_dim=shard_dim)
+    homes = plan.homes()
+    ho, hs, rs = plan.home_layout()
+    shards = [[_rank_piece(t, S, shard_dim, r) for t in ts] for r in range(S)]
+    rank_in = [torch.cat(sh).to(dev) if sh else torch.zeros(1, dtype=torch.bfloat16, device=dev) for sh in shards]
+
+    def bufs():
+        return ([torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs],
+                [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs],
+                [torch.full_like(x, 7.0) for x in rank_in])
+
+    hi1, ho1, ro1 = bufs()
+    ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+    ins = [hi1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))]
+    outs = [ho1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))]
+    nsg.ns_pack_to_home(plan, rank_in, hi1)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    nsg.ns_unpack_from_home(plan, ho1, ro1)
+    hi2, ho2, ro2 = bufs()
+    pipe = nsg.ns_pipeline_create(plan, n_waves)
+    pws = torch.empty(max(1, pipe.workspace_bytes), dtype=torch.uint8, device=dev)
+    nsg.ns_pipeline_run(pipe, rank_in, hi2, ho2, ro2, pws)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for a, b in zip(ro1, ro2):
+        assert torch.equal(a, b)
+    return ts, ho1, homes, ho
+
+
+def _rank_piece(t, S, shard_dim, r):
+    # rank r's (…, D/S, …) slice of t along shard_dim, flattened (torch.chunk)
+    return torch.chunk(t, S, dim=shard_dim)[r].contiguous().reshape(-1)
+
+
+@pytest.mark.parametrize("n_waves", [1, 3])
+def test_pipeline_ragged_shapes_fused_paths(n_waves):
+    # row shards along dim 0 take the fused paths (prologue reading the rank
+    # buffers, last B*X writing them); odd column counts and shard offsets
+    # exercise the unaligned fallbacks of both, tall shapes the transposed ones
+    from gpu_util import BF16_TOL, oracle_ns, rel_err
+    shapes = [(8, 5), (16, 3), (24, 40), (40, 24), (8, 7, 3), (200, 130), (136, 72), (64, 64)]
+    ts, ho1, homes, ho = _pipeline_vs_serial(shapes, 8, 0, n_waves, 91)
+    for i, t in enumerate(ts):
+        y = ho1[homes[i]][ho[i]:ho[i] + t.numel()].reshape(t.shape)
+        assert rel_err(y, oracle_ns(t)) <= BF16_TOL, shapes[i]
+
+
+def test_pipeline_shard_dim1_keeps_pack_and_unpack():
+    # shards along dim 1 are not contiguous rows: the pipeline packs and
+    # unpacks through the home buffers, with the same result as the serial calls
+    _pipeline_vs_serial([(64, 256), (256, 64), (128, 128), (96, 32)], 4, 1, 2, 92)
