@@ -190,7 +190,10 @@ const char* ns_status_string(int status);
  * steps of A = X X^T; X = a X + (b A + c A A) X, transposed back and stored.
  * workspace must hold ns_plan_workspace_bytes() bytes, 256-byte aligned; it
  * is scratch (no contents kept between calls). Asynchronous on `stream`;
- * calls that share a workspace must not overlap on the GPU. */
+ * calls that share a workspace must not overlap on the GPU. After a first
+ * call on a device (it looks up per-device state), the call may be captured
+ * into a CUDA graph and replayed: it allocates, synchronises and queries
+ * nothing; a replay reads the buffers' current contents. */
 int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const* out, int n,
                              void* workspace, uint64_t workspace_bytes, void* stream);
 
