@@ -333,12 +333,15 @@ def run_reference(args):
     if rank != 0:
         return
     w = get_workload(args.workload, args.layers)
+    # each step is a bounded sample: the whole run stays near 150 s of oracle
+    # work whatever --steps and --warmup are
+    budget = min(args.oracle_budget, max(2.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, args.oracle_budget)
+        cpu_oracle_sample(w, budget)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, threads, sample = cpu_oracle_sample(w, args.oracle_budget)
+        v, threads, sample = cpu_oracle_sample(w, budget)
         vals.append(v)
     wall = time.perf_counter() - t0
     v = statistics.median(vals)
