@@ -247,16 +247,27 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
                   if (cg + j < B.n_valid) dst[j] = hv[j];
               }
             } else {
-              // transposed: output rows cg .. cg + 31, walked without dividing
+              // transposed: output rows cg .. cg + 31
               const int sh = B.n_valid / p.S;
               int rk = cg / sh, lr = cg - rk * sh;
+              if (lr + 32 <= sh) {
+                // all 32 rows in one shard (always when sh is a multiple of
+                // 32): one base pointer, contiguous stores as for a tensor
+                __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.rank_ptr[rk]) + off +
+                                   static_cast<long long>(lr) * B.m_valid + r;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if (cg + j < B.n_valid)
-                  reinterpret_cast<__nv_bfloat16*>(p.rank_ptr[rk])[off + static_cast<long long>(lr) * B.m_valid + r] = hv[j];
-                if (++lr == sh) {
-                  ++rk;
-                  lr = 0;
+                for (int j = 0; j < 32; ++j)
+                  if (cg + j < B.n_valid) o[static_cast<long long>(j) * B.m_valid] = hv[j];
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (cg + j < B.n_valid)
+                    reinterpret_cast<__nv_bfloat16*>(p.rank_ptr[rk])[off + static_cast<long long>(lr) * B.m_valid + r] =
+                        hv[j];
+                  if (++lr == sh) {
+                    ++rk;
+                    lr = 0;
+                  }
                 }
               }
             }
