@@ -1,4 +1,4 @@
-// Launch parameters shared by the host orchestration (api.cu) and the kernels
+// Launch parameters shared by the host orchestration (orchestrate.h) and the kernels
 // (gemm.cu, prologue.cu, pack.cu), and the launcher entry points. Everything a
 // kernel needs per call travels by value in its parameter block, so the
 // Newton-Schulz path itself allocates nothing.
