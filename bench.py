@@ -390,7 +390,9 @@ def run_ours(args):
         for r in range(S):
             rank_host[r][pos:pos + n].copy_(t[r])
         pos += n
-    out_host = [torch.empty(L, dtype=torch.bfloat16, pin_memory=True) for _ in range(S)]
+    # pinned buffers are touched by the CPU once: untouched pinned pages make the
+    # first device -> host copy into them run at a fraction of the link speed
+    out_host = [torch.zeros(L, dtype=torch.bfloat16, pin_memory=True) for _ in range(S)]
 
     rank_in = [h.to(dev) for h in rank_host]
     home_in = [torch.empty(max(1, n), dtype=torch.bfloat16, device=dev) for n in home_sizes]
@@ -509,7 +511,7 @@ def run_ours(args):
         s_out = torch.cuda.Stream(dev)
         rin = [rank_in, [torch.empty_like(x) for x in rank_in]]
         rout = [rank_out, [torch.empty_like(x) for x in rank_out]]
-        hout = [out_host, [torch.empty_like(x, pin_memory=True) for x in out_host]]
+        hout = [out_host, [torch.zeros_like(x, pin_memory=True) for x in out_host]]
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_cmp = [torch.cuda.Event(), torch.cuda.Event()]
         ev_out = [torch.cuda.Event(), torch.cuda.Event()]
