@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above is set-up; the data path starts after the predecessor
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -273,17 +276,19 @@ cudaError_t launch_one(const P& p, int work_items, int nsm, cudaStream_t st) {
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
   if (CL == 1) {
     cfg.gridDim = dim3(static_cast<unsigned>(std::min(work_items, nsm)));
-    cfg.numAttrs = 0;
-  } else {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
+  } else {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(CL * (nsm / CL)));
     int max_clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);

@@ -139,6 +139,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
   cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above is set-up; the data path starts after the predecessor
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -241,13 +244,15 @@ cudaError_t launch_pair(const P& p, int work_items, int nsm, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;

@@ -19,6 +19,7 @@
 // issuing thread (tcgen05.mma.cta_group::1.kind::tf32, M=128, N=256, K=8),
 // two TMEM accumulators, four epilogue warps; every wait is bounded.
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace nsk {
@@ -118,6 +119,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm32_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above is set-up; the data path starts after the predecessor
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -348,7 +352,8 @@ cudaError_t launch32(const P& p, int grid, cudaStream_t st) {
   auto kern = ns_gemm32_kernel<PHASE, FINAL, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  e = launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, st, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -356,6 +361,8 @@ cudaError_t launch32(const P& p, int grid, cudaStream_t st) {
 // reduction). Standard step: A <- A + r I on the (hi, lo) pair. Gram-space
 // step (coef set): write that matrix's Q coefficients instead.
 __global__ void __launch_bounds__(256) ns_ridge32_kernel(const __grid_constant__ Ridge32Params p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const Ridge32Bucket& B = p.bk[blockIdx.y];
   if (static_cast<int>(blockIdx.x) >= B.count) return;
   float* ah = B.ah + static_cast<long long>(blockIdx.x) * B.mat_stride;
@@ -414,7 +421,8 @@ cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int grid, cudaStream
 
 cudaError_t launch_ridge32(const Ridge32Params& p, cudaStream_t st) {
   if (p.nb <= 0 || p.max_count <= 0) return cudaSuccess;
-  ns_ridge32_kernel<<<dim3(p.max_count, p.nb), 256, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(ns_ridge32_kernel, dim3(p.max_count, p.nb), dim3(256), 0, st, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

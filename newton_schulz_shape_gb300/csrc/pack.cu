@@ -26,6 +26,8 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "launch.cuh"
+#include "ptx.cuh"
 #include "status.h"
 
 namespace nsk {
@@ -77,6 +79,8 @@ __device__ __forceinline__ void copy_run(char* dst, const char* src, long long b
 }
 
 __global__ void __launch_bounds__(PACK_THREADS) ns_pack_kernel(const __grid_constant__ PackParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   const int r = blockIdx.y;
   // entry coordinates: per-rank positions (row-shard, two-stage) or global
   // positions (flat); this rank's share of [g_begin, g_end) in its own buffer
@@ -138,7 +142,9 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t st) {
   if (p.rank_len <= 0 || p.n_entries <= 0 || p.S <= 0 || p.g_end <= p.g_begin) return cudaSuccess;
   const long long span = std::min(p.rank_len, p.g_end - p.g_begin);  // positions per rank at most
   const long long nchunks = (span + p.chunk - 1) / p.chunk + (p.flat ? 1 : 0);
-  ns_pack_kernel<<<dim3(static_cast<unsigned>(nchunks), p.S), PACK_THREADS, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(ns_pack_kernel, dim3(static_cast<unsigned>(nchunks), p.S), dim3(PACK_THREADS), 0,
+                                  st, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "launch.cuh"
+#include "ptx.cuh"
 #include "status.h"
 
 namespace nsk {
@@ -40,6 +42,8 @@ __device__ __forceinline__ float block_sum(float v) {
 }
 
 __global__ void __launch_bounds__(SUMSQ_THREADS) ns_sumsq_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   const MatDesc& d = p.md[blockIdx.y];
   const long long c0 = static_cast<long long>(blockIdx.x) * SUMSQ_CHUNK;
   if (c0 >= d.numel) return;
@@ -74,6 +78,8 @@ __global__ void __launch_bounds__(SUMSQ_THREADS) ns_sumsq_kernel(const __grid_co
 }
 
 __global__ void __launch_bounds__(256) ns_scale_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   const MatDesc& d = p.md[blockIdx.x];
   double s = 0.0;
   for (int i = threadIdx.x; i < p.nchunks; i += blockDim.x) s += static_cast<double>(d.partial[i]);
@@ -120,6 +126,8 @@ __device__ __forceinline__ float sq8(const uint4& q) {
 constexpr int PREP_THREADS = 256;
 
 __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   const MatDesc& d = p.md[blockIdx.y];
   const unsigned short* __restrict__ src = reinterpret_cast<const unsigned short*>(d.in);
   uint4* __restrict__ x4 = reinterpret_cast<uint4*>(d.x);
@@ -233,6 +241,8 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
 
 // One 64 x 64 tile of the output (rows x cols) per CTA.
 __global__ void __launch_bounds__(256) ns_store_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   __shared__ float tile[TILE][TILE + 1];
   const MatDesc& d = p.md[blockIdx.y];
   const int rows = d.rows, cols = d.cols;
@@ -284,6 +294,8 @@ __device__ __forceinline__ float tf32_round(float x) {
 // fp32-Gram prologue: one 64 x 64 tile of X_0 = scale * V per CTA, written as
 // hi/lo TF32 pairs both as X (m_pad x n_pad) and as X^T (n_pad x m_pad).
 __global__ void __launch_bounds__(256) ns_prep32_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   __shared__ float tile[TILE][TILE + 1];
   const MatDesc& d = p.md[blockIdx.y];
   const float s = *d.scale;
@@ -325,6 +337,8 @@ __global__ void __launch_bounds__(256) ns_prep32_kernel(const __grid_constant__ 
 // fp32-Gram store (used when the last B*X launch could not store directly):
 // out (rows x cols, fp32) from X_k = hi + lo.
 __global__ void __launch_bounds__(256) ns_store32_kernel(const __grid_constant__ ProParams p) {
+  nsptx::griddep_wait();
+  nsptx::griddep_launch_dependents();
   __shared__ float tile[TILE][TILE + 1];
   const MatDesc& d = p.md[blockIdx.y];
   const int rows = d.rows, cols = d.cols;
@@ -366,7 +380,10 @@ __global__ void __launch_bounds__(256) ns_store32_kernel(const __grid_constant__
 cudaError_t launch_prep32(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
   const int tiles = (p.m_pad / TILE) * (p.n_pad / TILE);
-  ns_prep32_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_prep32_kernel, dim3(tiles, p.count), dim3(256), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -374,19 +391,28 @@ cudaError_t launch_store32(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
   const int rows = p.md[0].rows, cols = p.md[0].cols;
   const int tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
-  ns_store32_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_store32_kernel, dim3(tiles, p.count), dim3(256), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0 || p.nchunks <= 0) return cudaSuccess;
-  ns_sumsq_kernel<<<dim3(p.nchunks, p.count), SUMSQ_THREADS, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_sumsq_kernel, dim3(p.nchunks, p.count), dim3(SUMSQ_THREADS), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_scale(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
-  ns_scale_kernel<<<p.count, 256, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_scale_kernel, dim3(p.count), dim3(256), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -394,7 +420,10 @@ cudaError_t launch_prep(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
   // one CTA per 64-row stripe of X~_0 (p.nchunks stripes per matrix)
   if (p.nchunks != p.m_pad / TILE) return cudaErrorInvalidValue;
-  ns_prep_kernel<<<dim3(p.m_pad / TILE, p.count), PREP_THREADS, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_prep_kernel, dim3(p.m_pad / TILE, p.count), dim3(PREP_THREADS), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -404,7 +433,10 @@ cudaError_t launch_store(const ProParams& p, cudaStream_t st) {
   // all matrices of a bucket have the same (rows, cols) up to a transpose,
   // so the tile count is the same for each
   const int tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
-  ns_store_kernel<<<dim3(tiles, p.count), 256, 0, st>>>(p);
+  {
+    const cudaError_t e = launch_pdl(ns_store_kernel, dim3(tiles, p.count), dim3(256), 0, st, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 

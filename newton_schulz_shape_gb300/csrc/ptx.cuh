@@ -92,6 +92,17 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialization: a kernel may
+// start (and do its set-up) while its predecessor in the stream still runs.
+// griddep_wait() returns once the predecessor has completed and its memory
+// operations are visible; nothing of the data path may be read or written
+// before it. griddep_launch_dependents() lets the successor start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
