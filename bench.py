@@ -503,31 +503,43 @@ def run_ours(args):
 
     # ---- end to end: every step copies its inputs host -> device (pinned),
     # runs pack -> NS -> unpack, and copies its results device -> host. The
-    # copies of step k+1 (in) and k-1 (out) run on their own streams while
-    # step k computes; device buffers are double-buffered.
+    # copies run on their own streams while other steps compute, through a
+    # ring of NB buffer sets (device inputs, device outputs, pinned host
+    # outputs): step k's input copy may start once step k - NB has read its
+    # set, so the copy streams can fall behind for a while (the shared host
+    # link stalls single copies for ~100 ms at times) and catch up without
+    # holding the GPU. NB is 2-4, as device and host memory allow.
     e2e = None
     if not args.no_e2e:
         s_in = torch.cuda.Stream(dev)
         s_out = torch.cuda.Stream(dev)
-        rin = [rank_in, [torch.empty_like(x) for x in rank_in]]
-        rout = [rank_out, [torch.empty_like(x) for x in rank_out]]
-        hout = [out_host, [torch.zeros_like(x, pin_memory=True) for x in out_host]]
-        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_cmp = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        set_dev = 2 * 2 * S * L                      # inputs + outputs, bf16
+        set_host = 2 * S * L
+        free_dev = torch.cuda.mem_get_info(dev)[0]
+        try:
+            host_ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+        except (ValueError, OSError):
+            host_ram = 4 * set_host
+        NB = max(2, min(4, 1 + int(0.5 * free_dev // set_dev), 1 + int(0.25 * host_ram // set_host)))
+        rin = [rank_in] + [[torch.empty_like(x) for x in rank_in] for _ in range(NB - 1)]
+        rout = [rank_out] + [[torch.empty_like(x) for x in rank_out] for _ in range(NB - 1)]
+        hout = [out_host] + [[torch.zeros_like(x, pin_memory=True) for x in out_host] for _ in range(NB - 1)]
+        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_cmp = [torch.cuda.Event() for _ in range(NB)]
+        ev_out = [torch.cuda.Event() for _ in range(NB)]
 
         def e2e_steps(n):
             for k in range(n):
-                b = k % 2
+                b = k % NB
                 with torch.cuda.stream(s_in):
-                    if k >= 2:
-                        s_in.wait_event(ev_cmp[b])     # rank_in[b] was read by step k-2
+                    if k >= NB:
+                        s_in.wait_event(ev_cmp[b])     # rin[b] was read by step k - NB
                     for r in range(S):
                         rin[b][r].copy_(rank_host[r], non_blocking=True)
                     ev_in[b].record(s_in)
                 stream.wait_event(ev_in[b])
-                if k >= 2:
-                    stream.wait_event(ev_out[b])       # rank_out[b] was copied out by step k-2
+                if k >= NB:
+                    stream.wait_event(ev_out[b])       # rout[b] was copied out by step k - NB
                 step(rin[b], rout[b])
                 ev_cmp[b].record(stream)
                 with torch.cuda.stream(s_out):
@@ -536,7 +548,7 @@ def run_ours(args):
                         hout[b][r].copy_(rout[b][r], non_blocking=True)
                     ev_out[b].record(s_out)
 
-        e2e_steps(2)                                    # warm-up of the pipeline
+        e2e_steps(NB)                                   # warm-up of the pipeline
         barrier()
         e2e_clocks = ClockSampler(uuid)
         e2e_clocks.start()
@@ -554,11 +566,12 @@ def run_ours(args):
         clk_e2e = e2e_clocks.stop()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
         # the results of the last step really came back
-        ok = all(torch.equal(hout[(args.steps - 1) % 2][r], rank_out[r].cpu()) for r in range(S))
+        ok = all(torch.equal(hout[(args.steps - 1) % NB][r], rank_out[r].cpu()) for r in range(S))
         nbytes = 2 * S * L
         e2e = {"value": job_value(n_mats, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
-               "pipelining": "copies of step k+1 (in) and k-1 (out) overlap step k's compute",
+               "pipelining": f"copies on their own streams overlap the compute of other steps; ring of {NB} "
+                             "buffer sets (device in/out, pinned host out)",
                "results_returned": ok, "copy_gbs": copy_gbs, "clocks": clk_e2e}
 
     # ---- roofline of the dominant kernel
