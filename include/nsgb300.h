@@ -193,7 +193,11 @@ const char* ns_status_string(int status);
  * calls that share a workspace must not overlap on the GPU. After a first
  * call on a device (it looks up per-device state), the call may be captured
  * into a CUDA graph and replayed: it allocates, synchronises and queries
- * nothing; a replay reads the buffers' current contents. */
+ * nothing; a replay reads the buffers' current contents. The library's kernels
+ * are launched with programmatic stream serialization: each may start its
+ * set-up while the previous kernel in the stream runs, and reads or writes no
+ * data before that kernel has completed, so ordering with the caller's work
+ * on `stream` is as for ordinary launches. */
 int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const* out, int n,
                              void* workspace, uint64_t workspace_bytes, void* stream);
 
