@@ -146,8 +146,8 @@ int finish(Plan& p, bool keep_homes = false) {
     b.off_a = take(abytes);
     b.off_b = take(abytes);
     // partial sums of squares per matrix: 32K-element chunks (fp32 paths) or
-    // 64-row stripes of the padded X_0 (bf16 path)
-    b.nchunks = f32 ? (b.m * b.n + kSumsqChunk - 1) / kSumsqChunk : b.m_pad / 64;
+    // blocks of 64 rows x 1024 columns of the padded X_0 (bf16 path)
+    b.nchunks = f32 ? (b.m * b.n + kSumsqChunk - 1) / kSumsqChunk : (b.m_pad / 64) * ((b.n_pad + 1023) / 1024);
     b.off_partial = take(cnt * uint64_t(b.nchunks) * 4);
     b.off_scale = take(cnt * 4);
     b.off_coef = take(cnt * 3 * 4);

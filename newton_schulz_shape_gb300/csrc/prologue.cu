@@ -3,7 +3,7 @@
 // normalise, transpose so rows <= cols; the result is transposed back).
 //
 //   ns_prep_kernel    bf16 path: X~_0 = T or T^T, zero-padded to m_pad x n_pad,
-//                     unscaled, and per-stripe partial sums of squares (one pass)
+//                     unscaled, and per-block partial sums of squares (one pass)
 //   ns_sumsq_kernel   fp32 paths: partial sums of squares over 32K-element chunks
 //   ns_scale_kernel   scale = 1 / (sqrt(sum of partials) + eps), fixed order
 //   ns_store_kernel   out = X_k (or X_k^T) cropped to the tensor's (rows, cols)
@@ -113,17 +113,19 @@ __device__ __forceinline__ float sq8(const uint4& q) {
 
 // bf16 prologue, one pass: V = T (rows <= cols) or T^T copied unscaled into
 // X~_0 (m_pad x n_pad, zero padded) and the sum of squares of each 64-row
-// stripe of V written to partial[stripe]. The scale 1 / (||T||_F + eps) is
+// block of V written to partial[block]. The scale 1 / (||T||_F + eps) is
 // applied by the first step's products (A = s^2 X~ X~^T, X_1 = s (a X~ + B X~)),
 // which equals running the step on X_0 = s X~. The input is bf16, so X~_0
-// holds it exactly. blockIdx.x = stripe of 64 rows of X~_0, blockIdx.y = matrix.
+// holds it exactly. blockIdx.x = block of 64 rows x 1024 columns of X~_0
+// (row-stripe major), blockIdx.y = matrix; small batches still fill the GPU.
 //
 // Plain: 16-byte vectors of T rows to X~_0 rows, four loads in flight per
-// thread. Transposed: the stripe is 64 columns of T, walked in 64 x 64 tiles
+// thread. Transposed: the block is 64 columns of T, walked in 64 x 64 tiles
 // (64 rows of T x 128 bytes in, 64 rows of X~_0 x 128 bytes out, both whole
 // lines per warp access) through a double-buffered bf16 tile in shared memory
 // (rows of 33 words: conflict-free writes, 2-way reads).
 constexpr int PREP_THREADS = 256;
+constexpr int PREP_COLS = 1024;  // X~_0 columns per CTA (a multiple of 64)
 
 __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_constant__ ProParams p) {
   nsptx::griddep_wait();
@@ -142,18 +144,23 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
   const bool base_aligned = p.from_ranks ? (p.ranks_aligned && d.rank_off % 8 == 0)
                                          : (reinterpret_cast<uintptr_t>(src) & 15) == 0;
   const int nv = p.n_pad / 8;  // 16-byte vectors per X~_0 row
-  const int i0 = blockIdx.x * TILE;
+  // this CTA: rows [i0, i0 + 64) of X~_0, columns [c0, c1) (a block of
+  // PREP_COLS, the last one shorter)
+  const int ncb = (p.n_pad + PREP_COLS - 1) / PREP_COLS;
+  const int i0 = (blockIdx.x / ncb) * TILE;
+  const int c0 = (blockIdx.x % ncb) * PREP_COLS, c1 = min(p.n_pad, c0 + PREP_COLS);
   float acc = 0.0f;
   if (!d.transposed) {
     const bool vec = (p.n % 8 == 0) && base_aligned;
-    const int total = TILE * nv;
+    const int nvb = (c1 - c0) / 8;  // vectors of a row in this column block
+    const int total = TILE * nvb;
     constexpr int U = 4;
     for (int base = threadIdx.x; base < total; base += U * PREP_THREADS) {
       uint4 q[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = base + u * PREP_THREADS;
-        const int i = i0 + v / nv, j0 = (v % nv) * 8;
+        const int i = i0 + v / nvb, j0 = c0 + (v % nvb) * 8;
         q[u] = make_uint4(0, 0, 0, 0);
         if (v < total && i < p.m) {
           const unsigned short* row = trow(i);
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
         const int v = base + u * PREP_THREADS;
         if (v < total) {
           acc += sq8(q[u]);
-          x4[static_cast<long long>(i0) * nv + v] = q[u];
+          x4[static_cast<long long>(i0 + v / nvb) * nv + c0 / 8 + v % nvb] = q[u];
         }
       }
     }
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
     // X~[i][j] = T[j][i], T row-major n x m (rows j, cols i)
     __shared__ uint32_t tile[2][TILE][TILE / 2 + 1];
     const bool vec = (p.m % 8 == 0) && base_aligned;
-    const int ntiles = p.n_pad / TILE;
+    const int jt0 = c0 / TILE, jt1 = c1 / TILE;  // X~_0 column tiles = T row tiles
     // each thread moves two 16-byte vectors per tile: vector q = threadIdx.x + 256 h
     auto load = [&](int jt, uint4 (&r)[2]) {
 #pragma unroll
@@ -204,8 +211,8 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
       }
     };
     uint4 r[2];
-    load(0, r);
-    for (int jt = 0; jt < ntiles; ++jt) {
+    load(jt0, r);
+    for (int jt = jt0; jt < jt1; ++jt) {
       const int buf = jt & 1;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(PREP_THREADS) ns_prep_kernel(const __grid_cons
         tile[buf][jj][iw + 3] = r[h].w;
       }
       __syncthreads();
-      if (jt + 1 < ntiles) load(jt + 1, r);  // next tile's loads overlap this tile's stores
+      if (jt + 1 < jt1) load(jt + 1, r);  // next tile's loads overlap this tile's stores
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int q = threadIdx.x + h * PREP_THREADS;
@@ -418,10 +425,12 @@ cudaError_t launch_scale(const ProParams& p, cudaStream_t st) {
 
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
-  // one CTA per 64-row stripe of X~_0 (p.nchunks stripes per matrix)
-  if (p.nchunks != p.m_pad / TILE) return cudaErrorInvalidValue;
+  // one CTA per 64-row stripe and 1024-column block of X~_0 (p.nchunks of
+  // them per matrix, each writing one partial sum of squares)
+  const int ncb = (p.n_pad + PREP_COLS - 1) / PREP_COLS;
+  if (p.nchunks != (p.m_pad / TILE) * ncb) return cudaErrorInvalidValue;
   {
-    const cudaError_t e = launch_pdl(ns_prep_kernel, dim3(p.m_pad / TILE, p.count), dim3(PREP_THREADS), 0, st, p);
+    const cudaError_t e = launch_pdl(ns_prep_kernel, dim3(p.nchunks, p.count), dim3(PREP_THREADS), 0, st, p);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
