@@ -40,16 +40,34 @@ struct ns_pipeline {
 
 namespace {
 
+void release(PipeDev& pd) {
+  for (cudaEvent_t e : pd.ev)
+    if (e) cudaEventDestroy(e);
+  pd.ev.clear();
+  for (cudaStream_t* s : {&pd.mem, &pd.gemm, &pd.out}) {
+    if (*s) cudaStreamDestroy(*s);
+    *s = nullptr;
+  }
+}
+
+// streams and events of one device, created on first use; all or nothing, so
+// a failed set-up is retried by the next call
 int pipe_device(ns_pipeline* pl, int d) {
   PipeDev& pd = pl->dev[d];
   if (pd.mem) return NS_OK;
-  if (cudaStreamCreateWithFlags(&pd.mem, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&pd.gemm, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&pd.out, cudaStreamNonBlocking) != cudaSuccess)
+  PipeDev nd;
+  bool ok = cudaStreamCreateWithFlags(&nd.mem, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&nd.gemm, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&nd.out, cudaStreamNonBlocking) == cudaSuccess;
+  if (ok) {
+    nd.ev.assign(4 + 2 * pl->W, nullptr);
+    for (cudaEvent_t& e : nd.ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (!ok) {
+    release(nd);
     return NS_ERR_CUDA;
-  pd.ev.assign(4 + 2 * pl->W, nullptr);
-  for (cudaEvent_t& e : pd.ev)
-    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return NS_ERR_CUDA;
+  }
+  pd = nd;
   return NS_OK;
 }
 
@@ -64,10 +82,15 @@ int ns_pipeline_create(ns_plan_t* plan, int n_waves, ns_pipeline_t** out) {
   const Plan& p = plan->p;
   if (p.gram_mode != NS_BF16) return NS_ERR_UNSUPPORTED;
   const int np = static_cast<int>(p.part.size());
-  const int W = std::max(1, std::min(n_waves, np));
   ns_pipeline* pl = new (std::nothrow) ns_pipeline();
   if (!pl) return NS_ERR_ARG;
   pl->base = plan;
+  if (np == 0) {
+    // nothing participates: no waves, and a run only orders the streams
+    *out = pl;
+    return NS_OK;
+  }
+  const int W = std::min(n_waves, np);
   // cost-balanced cut of the participating tensors (index order) into W waves
   double total = 0;
   for (int i : p.part) total += static_cast<double>(std::max<int64_t>(p.t[i].cost, 1));
@@ -198,11 +221,7 @@ int ns_pipeline_destroy(ns_pipeline_t* pl) {
       PipeDev& pd = pl->dev[d];
       if (!pd.mem) continue;
       if (cudaSetDevice(d) != cudaSuccess) continue;
-      for (cudaEvent_t e : pd.ev)
-        if (e) cudaEventDestroy(e);
-      cudaStreamDestroy(pd.mem);
-      cudaStreamDestroy(pd.gemm);
-      cudaStreamDestroy(pd.out);
+      release(pd);
     }
     if (have) cudaSetDevice(cur);
   }

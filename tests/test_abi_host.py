@@ -272,3 +272,15 @@ def test_pipeline_wave_split_host():
     with pytest.raises(nsg.NsError) as e:
         nsg.ns_pipeline_create(fp32, 2)
     assert e.value.code == nsg.NS_ERR_UNSUPPORTED
+
+
+def test_pipeline_with_nothing_participating():
+    # a plan without participating tensors gives a pipeline of no waves
+    for plan in (nsg.ns_plan_create([], S=2),
+                 nsg.ns_plan_create_flat([(4, 4)], [0], 16, participating=[False], S=1)):
+        pipe = nsg.ns_pipeline_create(plan, 3)
+        assert pipe.n_waves == 0
+        assert pipe.workspace_bytes == 0
+    with pytest.raises(nsg.NsError) as e:
+        nsg.ns_pipeline_create(nsg.ns_plan_create([(8, 8)], S=1), 0)
+    assert e.value.code == nsg.NS_ERR_ARG
