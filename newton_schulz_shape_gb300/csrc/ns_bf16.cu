@@ -213,7 +213,7 @@ size_t group_matrices(const Plan& p, size_t b0, size_t b1) {
 // then unused.
 int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* ws, unsigned int* status,
                   cudaStream_t st, const void* const* rank_in) {
-  // prologue: X~_0 = T or T^T (unscaled, zero padded) with per-stripe sums of
+  // prologue: X~_0 = T or T^T (unscaled, zero padded) with per-block sums of
   // squares in one pass, then the scales
   for (const Bucket& b : p.buckets) {
     const BucketPtrs q = bucket_ptrs(b, ws);

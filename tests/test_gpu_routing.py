@@ -329,3 +329,22 @@ def test_pipeline_shard_dim1_keeps_pack_and_unpack():
     # shards along dim 1 are not contiguous rows: the pipeline packs and
     # unpacks through the home buffers, with the same result as the serial calls
     _pipeline_vs_serial([(64, 256), (256, 64), (128, 128), (96, 32)], 4, 1, 2, 92)
+
+
+def test_pipeline_with_no_participating_tensor_is_a_no_op():
+    # a flat plan in which nothing participates: no waves, the run only orders
+    # the streams and leaves every buffer as it was
+    dev = torch.device("cuda:0")
+    plan = nsg.ns_plan_create_flat([(4, 4)], [0], 16, participating=[False], S=2)
+    pipe = nsg.ns_pipeline_create(plan, 2)
+    assert pipe.n_waves == 0
+    bufs = [torch.full((8,), float(r + 1), dtype=torch.bfloat16, device=dev) for r in range(2)]
+    homes = [torch.full((1,), -1.0, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out = [torch.zeros(8, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ws = torch.empty(max(1, pipe.workspace_bytes), dtype=torch.uint8, device=dev)
+    nsg.ns_pipeline_run(pipe, bufs, homes, homes, out, ws)
+    torch.cuda.synchronize()
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    for r in range(2):
+        assert torch.equal(out[r], torch.zeros_like(out[r]))
+        assert torch.equal(bufs[r], torch.full_like(bufs[r], float(r + 1)))
