@@ -23,9 +23,10 @@ the Megatron-LM GitHub issue "[GTP][Muon] Optimize Muon step performance"
 
 Pinning status: every function here is pinned by a ``-m "not gpu"`` test
 against the pages' worked example, closed forms, library routines or brute
-force, except the trace-ridge term of ``ns.newton_schulz`` (``ridge > 0``),
-whose placement and scale are a reading, not a statement of the pages:
-parity unpinned for ``ridge > 0``.
+force. The trace-ridge term of ``ns.newton_schulz`` (``ridge > 0``) is pinned
+to the singular-value closed form of its reading (A <- A + ridge * tr(A)/m * I
+before B is formed); the placement and scale themselves are that reading, as
+the issue names a trace ridge without giving its form.
 """
 
 from . import ns, planning, routing  # noqa: F401

@@ -20,8 +20,9 @@ Readings where the page is silent (each is listed in the design notes):
   ``route_from_ns_home`` (page ``core.optimizer.layer_sharded_a2a``) hands
   out (P/S, Q) shards of a (P, Q) result;
 * optional trace ridge (issue #6720 pairs an fp32/TF32 Gram with a trace ridge):
-  A <- A + ridge * (trace(A) / m) * I before B is formed. ``ridge > 0`` is
-  parity unpinned: the issue names the ridge but not its form.
+  A <- A + ridge * (trace(A) / m) * I before B is formed. The issue names
+  the ridge but not its form; the oracle's ridge is pinned to the
+  singular-value closed form of this reading.
 
 The matrix products use numpy's float64 matmul (a library primitive); the
 operation order is exactly the page's, with no fusion or reordering.

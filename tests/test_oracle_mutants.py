@@ -1,8 +1,8 @@
 """Planted mistakes: each copy of the oracle below carries one plausible
 error, and at least one of the pins used on the real oracle must reject it.
 This shows the pins are strong enough to catch a dropped term, a wrong sign,
-a transposed operand, a wrong view, a wrong normalisation or a wrong
-tie-break -- on the CPU, never on a GPU.
+a transposed operand, a wrong view, a wrong normalisation, a misplaced
+trace ridge or a wrong tie-break -- on the CPU, never on a GPU.
 """
 
 import math
@@ -12,7 +12,7 @@ import pytest
 
 from oracle import ns as ons
 from oracle import planning as op
-from test_oracle_ns import A, B, C, EPS, svd_closed_form, scalar_map, rel
+from test_oracle_ns import A, B, C, EPS, svd_closed_form, ridge_closed_form, scalar_map, rel
 from test_oracle_planning import load
 
 
@@ -136,3 +136,58 @@ def test_real_lpt_passes_pins():
                               "reverse index on cost tie"])
 def test_lpt_mutant_is_caught(kw):
     assert not lpt_pins_pass(lambda w: lpt_variant(w, **kw))
+
+
+def ridge_variant(t, k, a, b, c, eps, lam, *, trace_over="m", where="gram"):
+    """The oracle's iteration with one planted mistake in the trace ridge."""
+    t = np.asarray(t, dtype=np.float64)
+    shape = t.shape
+    g = t.reshape(shape[0], -1)
+    tr = g.shape[0] > g.shape[1]
+    x = g.T if tr else g
+    x = x / (math.sqrt(float(np.sum(x * x))) + eps)
+    m, n = x.shape
+    for _ in range(k):
+        gm = x @ x.T
+        d = {"m": m, "n": n, "one": 1}[trace_over]
+        r = lam * np.trace(gm) / d
+        if where == "gram":
+            gr = gm + r * np.eye(m)
+            p = b * gr + c * (gr @ gr)
+        elif where == "linear_only":          # mistake: A^2 taken without the ridge
+            p = b * (gm + r * np.eye(m)) + c * (gm @ gm)
+        else:                                 # mistake: ridge added to B, not to A
+            p = b * gm + c * (gm @ gm) + r * np.eye(m)
+        x = a * x + p @ x
+    if tr:
+        x = x.T
+    return x.reshape(shape)
+
+
+def ridge_pins_pass(fn) -> bool:
+    rng = np.random.default_rng(321)
+    for shape in [(24, 60), (60, 24), (6, 2, 5)]:
+        for lam in (1e-5, 0.05):
+            t = rng.standard_normal(shape)
+            if rel(fn(t, 5, A, B, C, EPS, lam), ridge_closed_form(t, 5, lam)) > 1e-10:
+                return False
+    return True
+
+
+def test_real_ridge_passes_pins():
+    assert ridge_pins_pass(lambda t, k, a, b, c, e, lam: ons.newton_schulz(t, k, a, b, c, e, ridge=lam))
+    assert ridge_pins_pass(lambda t, k, a, b, c, e, lam: ridge_variant(t, k, a, b, c, e, lam))
+
+
+RIDGE_MUTANTS = {
+    "trace divided by n": dict(trace_over="n"),
+    "trace not divided": dict(trace_over="one"),
+    "A^2 without the ridge": dict(where="linear_only"),
+    "ridge added to B": dict(where="poly"),
+}
+
+
+@pytest.mark.parametrize("name", list(RIDGE_MUTANTS))
+def test_ridge_mutant_is_caught(name):
+    kw = RIDGE_MUTANTS[name]
+    assert not ridge_pins_pass(lambda t, k, a, b, c, e, lam: ridge_variant(t, k, a, b, c, e, lam, **kw))

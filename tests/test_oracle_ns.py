@@ -3,7 +3,8 @@
 Each check compares the oracle with something other than itself: the
 singular-value closed form (numpy's SVD as an independent library routine),
 the scalar map on diagonal inputs, orthogonal equivariance, transpose
-symmetry, a pure-Python brute force on tiny inputs, and the zero matrix.
+symmetry, a pure-Python brute force on tiny inputs, the zero matrix, and the
+singular-value form of the trace ridge.
 ``test_oracle_mutants.py`` plants plausible mistakes in copies of the oracle
 and shows that these pins catch each one.
 
@@ -138,6 +139,37 @@ def test_ridge_zero_is_plain():
     x = rng.standard_normal((10, 30))
     assert np.array_equal(ons.newton_schulz(x, 5, A, B, C, EPS, ridge=0.0),
                           ons.newton_schulz(x, 5, A, B, C, EPS))
+
+
+def ridge_closed_form(t, k, lam, eps=EPS, a=A, b=B, c=C):
+    """NS_k with the trace ridge (A <- A + lam tr(A)/m I before B) through the
+    SVD G = U diag(sigma) V^T: A's eigenvalues are sigma_i^2 and tr(A) is their
+    sum over the m = min(rows, cols) singular values, so every step is the
+    coupled scalar map sigma_i <- a sigma_i + (b q_i + c q_i^2) sigma_i with
+    q_i = sigma_i^2 + lam * mean(sigma^2)."""
+    t = np.asarray(t, dtype=np.float64)
+    g = t.reshape(t.shape[0], -1)
+    u, s, vt = np.linalg.svd(g, full_matrices=False)
+    nu = math.sqrt(float(np.sum(s * s))) + eps
+    sig = [float(x) / nu for x in s]
+    m = len(sig)
+    for _ in range(k):
+        r = lam * sum(x * x for x in sig) / m
+        sig = [a * x + (b * (x * x + r) + c * (x * x + r) ** 2) * x for x in sig]
+    return ((u * np.array(sig)) @ vt).reshape(t.shape)
+
+
+@pytest.mark.parametrize("shape", [(24, 60), (60, 24), (16, 16), (6, 2, 5)])
+@pytest.mark.parametrize("lam", [1e-5, 0.05])
+def test_ridge_closed_form(shape, lam):
+    # the trace ridge of the fp32-Gram mode, pinned to its singular-value
+    # closed form (a large lam as well, so a wrong trace scale shows)
+    rng = np.random.default_rng(abs(hash((shape, lam))) % 2**32)
+    t = rng.standard_normal(shape)
+    got = ons.newton_schulz(t, 5, A, B, C, EPS, ridge=lam)
+    assert rel(got, ridge_closed_form(t, 5, lam)) < 1e-10
+    if lam >= 0.05:
+        assert rel(got, svd_closed_form(t, 5)) > 1e-3   # the ridge changes the result
 
 
 def test_useful_flops():
