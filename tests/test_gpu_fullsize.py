@@ -8,13 +8,19 @@ matrices (one per (m, n) bucket, first and last tensor):
   * unpack: every rank buffer holds its shard of the result, bit for bit.
 Every matrix is also checked for properties that hold at any size: finite,
 and ||Y||_F / sqrt(m) inside the band the 5-step map allows for these inputs.
+At the sweep's largest size, where the oracle cannot run in seconds, a
+structured input with orthogonal rows is checked against its closed form
+(tied to the oracle on small sizes by test_closed_form_inputs.py).
 """
+
+import math
 
 import numpy as np
 import pytest
 import torch
 
 import workloads
+from closed_forms import hadamard_row_norms, row_gains
 from gpu_util import BF16_TOL, bits, oracle_ns, rel_err
 
 pytestmark = pytest.mark.gpu
@@ -119,3 +125,41 @@ def test_sweep_conv_3d():
 def test_sweep_8192_square():
     w = workloads.sweep_shapes(8192, 1, 1)
     run_pipeline(w, sample=[0])
+
+
+def test_max_sweep_size_closed_form():
+    # the sweep's largest matrix, 8192 x 65536 (1 GiB of bf16), wide and tall
+    # in one batch, against the closed form NS_k(X)_i = g_i X_i of an input
+    # with orthogonal rows. Checked per matrix (relative Frobenius error, the
+    # bf16 bar) and per 128 x 256 output tile, so that one wrong tile anywhere
+    # in the 2^29 elements fails.
+    dev = torch.device("cuda:0")
+    m, blocks = 8192, 8
+    x, r, d = workloads.gen_hadamard_rows(m, blocks, seed=5807, device="cuda")
+    shapes = [(m, m * blocks), (m * blocks, m)]
+    ins = [x, x.t().contiguous()]
+    outs = [torch.empty_like(t) for t in ins]
+    plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=1)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    del ws
+    g = torch.tensor(row_gains(hadamard_row_norms(m, r, d), workloads.STEPS, workloads.A_COEF,
+                               workloads.B_COEF, workloads.C_COEF, workloads.EPS),
+                     dtype=torch.float64, device=dev)
+    for y, tall in zip(outs, (False, True)):
+        yw = y.t() if tall else y
+        num = den = 0.0
+        worst_tile = 0.0
+        for i0 in range(0, m, 1024):
+            want = g[i0:i0 + 1024, None] * x[i0:i0 + 1024].double()
+            diff = yw[i0:i0 + 1024].double() - want
+            num += float(diff.square().sum())
+            den += float(want.square().sum())
+            dt = diff.square().reshape(8, 128, -1, 256).sum(dim=(1, 3))
+            wt = want.square().reshape(8, 128, -1, 256).sum(dim=(1, 3))
+            worst_tile = max(worst_tile, float((dt / wt).sqrt().max()))
+            del want, diff
+        err = math.sqrt(num / den)
+        assert err <= BF16_TOL, (tall, err)
+        assert worst_tile <= 0.1, (tall, worst_tile)

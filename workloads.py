@@ -144,3 +144,38 @@ def split_rows(shapes, splits=None):
             parents.append((i, r0))
             r0 += rows
     return out, parents
+
+
+def gen_hadamard_rows(m: int, blocks: int, seed: int, device: str = "cpu"):
+    """Seeded structured input with orthogonal rows, for closed-form checks at
+    sizes the float64 oracle cannot run in seconds.
+
+    X (m x blocks*m, m a power of two) is `blocks` column blocks; block j is
+    d_j * diag(r) * P * H_m * Q_j, where H_m is the Sylvester Hadamard matrix
+    (entry (i, k) = (-1)^popcount(i & k)), P a seeded row permutation, Q_j a
+    seeded signed column permutation, and r_i, d_j are drawn from
+    {1, 1.125, ..., 1.875}. Every entry is +-(8 + u)(8 + v) / 64 with
+    u, v < 8: at most 8 significant bits, so X is exact in bf16.
+    Returns (X as bf16 on `device`, r, d) with r and d as lists of floats.
+    The seeded draws come from numpy; the rest is integer and exact float
+    arithmetic, so every device gives the same bits.
+    """
+    import numpy as np
+
+    if m < 1 or m & (m - 1):
+        raise ValueError("m must be a power of two")
+    rng = np.random.default_rng(seed)
+    r = (8 + rng.integers(0, 8, m)) / 8.0
+    d = (8 + rng.integers(0, 8, blocks)) / 8.0
+    rows = torch.from_numpy(rng.permutation(m).astype(np.int32)).to(device)
+    r_t = torch.from_numpy(r.astype(np.float32)).to(device)
+    out = torch.empty((m, blocks * m), dtype=torch.bfloat16, device=device)
+    for j in range(blocks):
+        cols = torch.from_numpy(rng.permutation(m).astype(np.int32)).to(device)
+        sign = torch.from_numpy((1 - 2 * rng.integers(0, 2, m)).astype(np.float32)).to(device)
+        v = rows[:, None] & cols[None, :]
+        for sh in (16, 8, 4, 2, 1):
+            v ^= v >> sh
+        mag = r_t[:, None] * (sign * float(d[j]))[None, :]        # exact: <= 8 significant bits
+        out[:, j * m:(j + 1) * m] = torch.where((v & 1).bool(), -mag, mag).to(torch.bfloat16)
+    return out, [float(x) for x in r], [float(x) for x in d]
