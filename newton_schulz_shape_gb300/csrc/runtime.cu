@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -24,7 +25,8 @@ unsigned int* g_status_ptr[nsplan::kMaxDevices] = {nullptr};
 int g_sm_count[nsplan::kMaxDevices] = {0};
 int g_cc_ok[nsplan::kMaxDevices] = {0};  // 0 unknown, 1 sm_103, -1 other
 
-EncodeTiledFn g_encode = nullptr;
+// set once under g_mu, read without it by every launch's tensor-map encoding
+std::atomic<EncodeTiledFn> g_encode{nullptr};
 int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
 
 // ----------------------------------------------------------- measurement
@@ -72,7 +74,7 @@ int gemm_cluster_override() {
   return g_force_cl;
 }
 
-EncodeTiledFn tensor_map_encoder() { return g_encode; }
+EncodeTiledFn tensor_map_encoder() { return g_encode.load(std::memory_order_acquire); }
 
 // Per-device set-up: status word address, SM count, architecture check.
 int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out) {
@@ -97,14 +99,14 @@ int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out) {
     g_cc_ok[dev] = 1;
   }
   if (g_cc_ok[dev] < 0) return NS_ERR_UNSUPPORTED;
-  if (!g_encode) {
+  if (!g_encode.load(std::memory_order_relaxed)) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
       return NS_ERR_CUDA;
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    g_encode.store(reinterpret_cast<EncodeTiledFn>(fn), std::memory_order_release);
   }
   *dev_out = dev;
   *status_out = g_status_ptr[dev];
@@ -118,7 +120,7 @@ int make_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_
   cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
   cuuint32_t box[3] = {box_inner, box_outer, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+  CUresult r = tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
