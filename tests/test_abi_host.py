@@ -32,6 +32,17 @@ def test_library_exports_every_header_symbol():
     assert sorted(_SIGS) == syms
 
 
+def test_header_constants_match_the_binding():
+    # every enumerator of the header has the same value in the binding
+    import re
+    from newton_schulz_shape_gb300 import _lib
+    hdr = open(os.path.join(os.path.dirname(GOLD), "..", "include", "nsgb300.h")).read()
+    consts = dict((k, int(v)) for k, v in re.findall(r"\b(NS_[A-Z0-9_]+)\s*=\s*(-?\d+)", hdr))
+    assert len(consts) >= 17
+    for k, v in consts.items():
+        assert getattr(_lib, k) == v, k
+
+
 def test_ns_cost_hand_values_and_oracle():
     with open(os.path.join(GOLD, "planning_hand_cases.json")) as f:
         cases = json.load(f)["ns_cost"]
