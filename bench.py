@@ -21,14 +21,14 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-
-import numpy as np
 import json
 import os
 import statistics
 import subprocess
 import sys
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
