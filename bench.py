@@ -52,8 +52,8 @@ def parse():
                     help="sweep subset, e.g. '1024x1,4096x8' (m x aspect); default: all")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
-    ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="GEMM tiling: 0 automatic, 1 single CTA, 2 multicast CTA pairs, 3 2-SM MMA")
+    ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 3],
+                    help="GEMM tiling: 0 automatic, 1 single CTA, 3 2-SM MMA")
     ap.add_argument("--waves", type=int, default=2,
                     help="run the step through the wave pipeline with this many waves (0: serial calls)")
     ap.add_argument("--split-qkv", action="store_true",

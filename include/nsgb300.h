@@ -283,14 +283,14 @@ int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, vo
  * stream it is launched on; ns_profile_read synchronises those events. */
 
 /* Tuning: how the bf16 GEMM phases use the tensor cores. cl = 1: one CTA per
- * 128 x 256 tile (tcgen05 cta_group::1); cl = 2: clusters of two such CTAs
- * sharing each B tile by TMA multicast; cl = 3: clusters of two CTAs running
+ * 128 x 256 tile (tcgen05 cta_group::1); cl = 3: clusters of two CTAs running
  * the 2-SM MMA (cta_group::2) on 256 x 256 tiles, each SM holding half of
  * each operand; cl = 0 (default) picks 3 for the Gram phase, and 3 for A*A
  * and B*X when every bucket has an even number of 128-row tile rows (else 1):
- * the fastest measured per phase. Paired modes apply to launches
- * whose buckets all have at least two 128-row tile rows; others use 1.
- * Process-wide; all modes give bitwise-identical results. */
+ * the fastest measured per phase. The paired mode applies to launches whose
+ * buckets all have at least two 128-row tile rows; others use 1. Any other
+ * value is NS_ERR_ARG. Process-wide; all modes give bitwise-identical
+ * results. */
 int ns_set_gemm_cluster(int cl);
 
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */

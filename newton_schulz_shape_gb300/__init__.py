@@ -250,7 +250,7 @@ def ns_profile_read(reset: bool = False):
 def ns_set_gemm_cluster(cl: int) -> None:
     """GEMM tiling: 0 automatic (2-SM MMA for the Gram, and for A*A and B*X when
     every bucket has an even number of 128-row tile rows), 1 single CTA,
-    2 multicast pairs, 3 2-SM MMA."""
+    3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")
 
 

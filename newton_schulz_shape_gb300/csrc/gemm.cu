@@ -27,6 +27,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace nsk {
@@ -43,14 +44,11 @@ constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 
 constexpr int THREADS = 192;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + EPI_RING_BYTES + 512;
 
-// Work item t -> (bucket b, matrix, output tile (tm, tn)). With CL = 2 a work
-// item is a pair of tile rows (2q, 2q + 1) sharing column tile tn; the CTA of
-// cluster rank `rank` takes row 2q + rank. SYRK phases visit only tiles that
-// touch the upper triangle: in tile row tm, column tiles from
-// floor(tm * BM / BN), which is q for both rows of a pair.
-template <int PHASE, int CL, typename P>
-__device__ __forceinline__ void decode_tile(const P& p, long long t, uint32_t rank, int& b, int& mat, int& tm,
-                                            int& tn) {
+// Work item t -> (bucket b, matrix, output tile (tm, tn)). SYRK phases visit
+// only tiles that touch the upper triangle: in tile row tm, column tiles from
+// floor(tm * BM / BN).
+template <int PHASE, typename P>
+__device__ __forceinline__ void decode_tile(const P& p, long long t, int& b, int& mat, int& tm, int& tn) {
   if (p.reverse) t = p.total_tiles - 1 - t;
   b = 0;
   while (b + 1 < p.nb && t >= p.bk[b + 1].tile_begin) ++b;
@@ -58,36 +56,28 @@ __device__ __forceinline__ void decode_tile(const P& p, long long t, uint32_t ra
   const long long local = t - B.tile_begin;
   mat = static_cast<int>(local / B.tiles_per_mat);
   int r = static_cast<int>(local % B.tiles_per_mat);
-  int q;
   if (PHASE == PH_BX) {
-    q = r / B.tiles_n;
+    tm = r / B.tiles_n;
     tn = r % B.tiles_n;
-  } else {
-    q = 0;
-    while (true) {
-      const int tn0 = CL == 1 ? (q * BM) / BN : q;
-      const int cnt = B.tiles_n - tn0;
-      if (r < cnt) {
-        tn = tn0 + r;
-        break;
-      }
-      r -= cnt;
-      ++q;
-    }
+    return;
   }
-  tm = CL == 1 ? q : 2 * q + static_cast<int>(rank);
+  tm = 0;
+  while (true) {
+    const int tn0 = (tm * BM) / BN;
+    const int cnt = B.tiles_n - tn0;
+    if (r < cnt) {
+      tn = tn0 + r;
+      return;
+    }
+    r -= cnt;
+    ++tm;
+  }
 }
 
 // FINAL (B*X phase only): write the cropped, transposed-back result to the
 // caller's tensors listed in p.out_tab instead of the next X buffer.
-// CL = 2: launched as clusters of two CTAs working on tile rows 2q and 2q + 1
-// of the same column tile; each CTA loads its own A tile and half of the
-// shared B tile, multicast to both, so per-SM operand traffic drops from 48 KB
-// to 32 KB per K-block. A stage is refilled only when both CTAs' MMAs have
-// released it (empty barriers count one arrival from each CTA).
-template <int PHASE, bool FINAL, int CL, typename P>
+template <int PHASE, bool FINAL, typename P>
 __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ P p) {
-  static_assert(CL == 1 || CL == 2, "cluster size 1 or 2");
   static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
   constexpr bool B_MN = (PHASE == PH_BX);
   constexpr uint32_t IDESC = idesc_make(1u, BM, BN, false, B_MN);
@@ -112,15 +102,13 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   }
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const uint32_t rank = CL == 1 ? 0u : cluster_ctarank();
-  const long long t0 = CL == 1 ? static_cast<long long>(blockIdx.x) : static_cast<long long>(cluster_id_x());
-  const long long tstride = CL == 1 ? static_cast<long long>(gridDim.x) : static_cast<long long>(cluster_count_x());
-  constexpr uint16_t MC_ALL = (1u << CL) - 1u;
+  const long long t0 = static_cast<long long>(blockIdx.x);
+  const long long tstride = static_cast<long long>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -143,7 +131,6 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // everything above is set-up; the data path starts after the predecessor
@@ -156,7 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     long long issued = 0;
     for (long long t = t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
-      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
@@ -164,28 +151,13 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
         uint8_t* a_dst = sA + stage * A_BYTES;
         uint8_t* b_dst = sB + stage * B_BYTES;
         tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
-        if (CL == 1) {
-          if (!B_MN) {
-            tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
-            tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
-          }
+        if (!B_MN) {
+          tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
+          tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
         } else {
-          // this CTA's half of the shared B tile, multicast to both CTAs
-          if (!B_MN) {
-            tma_load_3d_mc(b_dst + rank * (128 * 128), &p.tmb[b], &full[stage], kb * BK,
-                           tn * BN + static_cast<int>(rank) * 128, mat, MC_ALL);
-          } else {
 #pragma unroll
-            for (int jj = 0; jj < BN / 128; ++jj) {
-              const int j = static_cast<int>(rank) * (BN / 128) + jj;
-              tma_load_3d_mc(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat,
-                             MC_ALL);
-            }
-          }
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
         }
         ++issued;
         if (++stage == STAGES) {
@@ -206,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     for (long long t = t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
-      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
       tc_fence_after();
@@ -223,10 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
           mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        if (CL == 1)
-          mma_commit(&empty[stage]);
-        else
-          mma_commit_mc(&empty[stage], MC_ALL);  // the stage is free once both CTAs are done with it
+        mma_commit(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -245,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     // -------------------------------------------------------------- epilogue
     const int lg = warp & 3;  // this warp may read TMEM lanes [32*lg, 32*lg + 32)
     auto dec = [&](long long t, int& b, int& mat, int& tm, int& tn) {
-      decode_tile<PHASE, CL>(p, t, rank, b, mat, tm, tn);
+      decode_tile<PHASE>(p, t, b, mat, tm, tn);
     };
     auto release = [&](uint32_t a) { mbar_arrive(&tempty[a]); };
     epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, tfull,
@@ -259,74 +228,35 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if (CL > 1) {
-    // no CTA leaves while its peer may still multicast into it or arrive on
-    // its barriers
-    __syncwarp();
-    cluster_sync_all();
-  }
 }
 
-template <int PHASE, bool FINAL, int CL, typename P>
+template <int PHASE, bool FINAL, typename P>
 cudaError_t launch_one(const P& p, int work_items, int nsm, cudaStream_t st) {
-  auto kern = ns_gemm_kernel<PHASE, FINAL, CL, P>;
+  auto kern = ns_gemm_kernel<PHASE, FINAL, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  if (CL == 1) {
-    cfg.gridDim = dim3(static_cast<unsigned>(std::min(work_items, nsm)));
-    cfg.numAttrs = 1;
-  } else {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = CL;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-    cfg.gridDim = dim3(static_cast<unsigned>(CL * (nsm / CL)));
-    int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    cfg.gridDim = dim3(static_cast<unsigned>(CL * std::min(work_items, max_clusters)));
-  }
-  e = cudaLaunchKernelEx(&cfg, kern, p);
+  e = launch_pdl(kern, dim3(static_cast<unsigned>(std::min(work_items, nsm))), dim3(THREADS), SMEM_BYTES, st, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int phase, int cl, const GemmParams& p, int nsm, cudaStream_t st) {
+cudaError_t launch_gemm(int phase, const GemmParams& p, int nsm, cudaStream_t st) {
   if (p.total_tiles <= 0) return cudaSuccess;
   const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
-  if (cl == 2) {
-    switch (phase) {
-      case PH_GRAM: return launch_one<PH_GRAM, false, 2>(p, items, nsm, st);
-      case PH_A2B: return launch_one<PH_A2B, false, 2>(p, items, nsm, st);
-      case PH_BX: return launch_one<PH_BX, false, 2>(p, items, nsm, st);
-      default: return cudaErrorInvalidValue;
-    }
-  }
   switch (phase) {
-    case PH_GRAM: return launch_one<PH_GRAM, false, 1>(p, items, nsm, st);
-    case PH_A2B: return launch_one<PH_A2B, false, 1>(p, items, nsm, st);
-    case PH_BX: return launch_one<PH_BX, false, 1>(p, items, nsm, st);
+    case PH_GRAM: return launch_one<PH_GRAM, false>(p, items, nsm, st);
+    case PH_A2B: return launch_one<PH_A2B, false>(p, items, nsm, st);
+    case PH_BX: return launch_one<PH_BX, false>(p, items, nsm, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gemm_final(int cl, const GemmFinalParams& p, int nsm, cudaStream_t st) {
+cudaError_t launch_gemm_final(const GemmFinalParams& p, int nsm, cudaStream_t st) {
   if (p.total_tiles <= 0) return cudaSuccess;
   const int items = static_cast<int>(std::min<long long>(p.total_tiles, 1 << 30));
-  if (cl == 2) return launch_one<PH_BX, true, 2>(p, items, nsm, st);
-  return launch_one<PH_BX, true, 1>(p, items, nsm, st);
+  return launch_one<PH_BX, true>(p, items, nsm, st);
 }
 
 }  // namespace nsk

@@ -193,13 +193,12 @@ struct PackParams {
 };
 
 // ----------------------------------------------------------------- launchers
-// cl = 1: one CTA per tile; cl = 2: clusters of two CTAs sharing the B tile
-// (p.bk[].tiles_per_mat then counts tile-row pairs). The launchers size the
-// grid from the work items, the SM count and cluster occupancy.
-cudaError_t launch_gemm(int phase, int cl, const GemmParams& p, int nsm, cudaStream_t st);
-cudaError_t launch_gemm_final(int cl, const GemmFinalParams& p, int nsm, cudaStream_t st);
+// 1-SM form: one CTA per 128 x 256 tile. The launchers size the grid from
+// the work items, the SM count and cluster occupancy.
+cudaError_t launch_gemm(int phase, const GemmParams& p, int nsm, cudaStream_t st);
+cudaError_t launch_gemm_final(const GemmFinalParams& p, int nsm, cudaStream_t st);
 // 2-SM form (tcgen05 cta_group::2): clusters of two CTAs compute 256 x 256
-// tiles; p.bk[].tiles_per_mat counts tile-row pairs as for cl = 2.
+// tiles; p.bk[].tiles_per_mat counts tile-row pairs.
 cudaError_t launch_gemm_pair(int phase, const GemmParams& p, int nsm, cudaStream_t st);
 cudaError_t launch_gemm_pair_final(const GemmFinalParams& p, int nsm, cudaStream_t st);
 cudaError_t launch_sumsq(const ProParams& p, cudaStream_t st);

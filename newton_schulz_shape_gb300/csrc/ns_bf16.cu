@@ -20,7 +20,7 @@
 namespace nsorch {
 
 // Upper-triangle work items of one matrix: single tiles (cl = 1) or pairs of
-// tile rows 2q, 2q + 1 sharing their column tiles (cl = 2).
+// tile rows 2q, 2q + 1 sharing their column tiles (cl = 2, the 2-SM MMA).
 long long syrk_tiles(int tiles_m, int tiles_n, int cl) {
   long long t = 0;
   if (cl == 1) {
@@ -33,10 +33,9 @@ long long syrk_tiles(int tiles_m, int tiles_n, int cl) {
 
 namespace {
 
-// GEMM tiling for a launch: 1 = one CTA per 128 x 256 tile; 2 = CTA pairs
-// sharing B tiles by multicast; 3 = CTA pairs running the 2-SM MMA on
-// 256 x 256 tiles. Pairs need every bucket of the launch to have at least two
-// tile rows.
+// GEMM tiling for a launch: 1 = one CTA per 128 x 256 tile; 3 = CTA pairs
+// running the 2-SM MMA on 256 x 256 tiles. Pairs need every bucket of the
+// launch to have at least two tile rows.
 int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   for (size_t bi = b0; bi < b1; ++bi) {
     const Bucket& b = p.buckets[bi];
@@ -54,7 +53,7 @@ int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   return 3;
 }
 
-// Work items per matrix count tile-row pairs for both paired modes.
+// Work items per matrix count tile-row pairs in the paired mode.
 int count_mode(int cl) { return cl == 1 ? 1 : 2; }
 
 }  // namespace
@@ -176,7 +175,7 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
   if (rc != NS_OK) return rc;
   gp.reverse = reverse ? 1 : 0;
   return counted(phase, st, [&] {
-           return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, cl, gp, nsm, st);
+           return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, gp, nsm, st);
          }) == cudaSuccess
              ? NS_OK
              : NS_ERR_CUDA;
@@ -192,7 +191,7 @@ int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, 
   gp.reverse = reverse ? 1 : 0;
   if (rc != NS_OK) return rc;
   return counted(K_BX_FINAL, st, [&] {
-           return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(cl, gp, nsm, st);
+           return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(gp, nsm, st);
          }) == cudaSuccess
              ? NS_OK
              : NS_ERR_CUDA;

@@ -156,7 +156,7 @@ int ns_check_status(ns_plan_t* /*plan*/, void* stream) {
 }
 
 int ns_set_gemm_cluster(int cl) {
-  if (cl < 0 || cl > 3) return NS_ERR_ARG;
+  if (cl != 0 && cl != 1 && cl != 3) return NS_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_cl = cl;
   return NS_OK;

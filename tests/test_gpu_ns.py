@@ -98,7 +98,7 @@ def test_repeatable_bitwise():
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("cl", [0, 1, 2, 3])
+@pytest.mark.parametrize("cl", [0, 1, 3])
 def test_cluster_pairs_odd_tile_rows(cl):
     # m_pad = 384, 384, 640: odd tile-row counts leave a spare CTA in the last pair
     shapes = [(300, 700), (700, 300), (640, 960), (256, 256)]
@@ -112,7 +112,7 @@ def test_cluster_pairs_odd_tile_rows(cl):
         assert rel_err(o, oracle_ns(t)) <= BF16_TOL, (cl, s_)
 
 
-@pytest.mark.parametrize("cl", [2, 3])
+@pytest.mark.parametrize("cl", [3])
 def test_cluster_and_single_cta_agree(cl):
     shapes = [(1024, 3072), (2048, 1024)]
     ts = workloads.gen_tensors(workloads.Workload("agree", shapes, 0.02, 18))
