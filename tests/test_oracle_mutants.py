@@ -191,3 +191,50 @@ RIDGE_MUTANTS = {
 def test_ridge_mutant_is_caught(name):
     kw = RIDGE_MUTANTS[name]
     assert not ridge_pins_pass(lambda t, k, a, b, c, e, lam: ridge_variant(t, k, a, b, c, e, lam, **kw))
+
+
+# ------------------------------------------------- the error measure
+def err_variant(y, y_ref, *, squared=False, den="ref", norm="fro"):
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    d = y - y_ref
+
+    def nrm(v):
+        if norm == "maxabs":
+            return float(np.max(np.abs(v))) if v.size else 0.0
+        if norm == "first_slice":                     # mistake: one row / slice only
+            return math.sqrt(float(np.sum(v.reshape(v.shape[0], -1)[0] ** 2)))
+        return math.sqrt(float(np.sum(v * v)))
+
+    base = {"ref": nrm(y_ref), "y": nrm(y), "sum": nrm(y) + nrm(y_ref)}[den]
+    if base == 0.0:
+        return nrm(d)
+    r = nrm(d) / base
+    return r * r if squared else r
+
+
+def err_pins_pass(fn) -> bool:
+    from test_oracle_ns import ERROR_HAND_CASES
+    for y, y_ref, want in ERROR_HAND_CASES:
+        if abs(fn(np.array(y), np.array(y_ref)) - want) > 1e-15 * max(1.0, want):
+            return False
+    return True
+
+
+def test_real_error_measure_passes_pins():
+    assert err_pins_pass(ons.rel_fro_error)
+
+
+ERR_MUTANTS = {
+    "squared ratio": dict(squared=True),
+    "||y|| as the denominator": dict(den="y"),
+    "||y|| + ||y_ref|| as the denominator": dict(den="sum"),
+    "max-abs instead of Frobenius": dict(norm="maxabs"),
+    "norm over the first row only": dict(norm="first_slice"),
+}
+
+
+@pytest.mark.parametrize("name", list(ERR_MUTANTS))
+def test_error_measure_mutant_is_caught(name):
+    kw = ERR_MUTANTS[name]
+    assert not err_pins_pass(lambda y, r: err_variant(y, r, **kw)), name

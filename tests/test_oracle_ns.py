@@ -177,3 +177,49 @@ def test_useful_flops():
     # 4*128*128*256 = 16777216, 2*128^3 = 4194304, sum 20971520, x5 = 104857600
     assert ons.useful_flops((128, 256), 5) == 104857600
     assert ons.useful_flops((256, 128), 5) == 104857600
+
+
+# --- the per-matrix error measure every parity verdict goes through --------
+# Hand-worked values of ||y - y_ref||_F / ||y_ref||_F (and ||y||_F when
+# y_ref = 0). Each case is chosen so that a plausible slip gives a different
+# number: the squared ratio, the wrong denominator (||y|| instead of
+# ||y_ref||), a max-abs or per-row norm, or a norm over one slice only.
+ERROR_HAND_CASES = [
+    # diff = [[3, 0], [0, -1]]: sqrt(9 + 1) = sqrt(10); ||y_ref|| = 5
+    ([[3.0, 0.0], [0.0, 4.0]], [[0.0, 0.0], [0.0, 5.0]], math.sqrt(10.0) / 5.0),
+    # diff = [[-1, 1]]: sqrt(2); ||y_ref|| = 2 (||y|| = sqrt(2) would give 1)
+    ([[1.0, 1.0]], [[2.0, 0.0]], math.sqrt(2.0) / 2.0),
+    # diff = [1, 1, 1, -1]: Frobenius 2 (max-abs 1); ||y_ref|| = 2
+    ([[1.0, 1.0, 1.0, 1.0]], [[0.0, 0.0, 0.0, 2.0]], 1.0),
+    # rows: row 0 exact, row 1 off by 3 against ||y_ref|| = sqrt(16 + 9) = 5
+    # (the mean of per-row errors would be (0 + 3/3) / 2 = 0.5)
+    ([[4.0, 0.0], [0.0, 6.0]], [[4.0, 0.0], [0.0, 3.0]], 3.0 / 5.0),
+    # a 3-D tensor: the norm runs over every element, not one slice
+    ([[[1.0, 0.0]], [[0.0, 2.0]]], [[[1.0, 0.0]], [[0.0, 0.0]]], 2.0),
+    # y_ref = 0: the absolute Frobenius norm of y, sqrt(1 + 4 + 4 + 16) = 5
+    ([[1.0, 2.0], [2.0, 4.0]], [[0.0, 0.0], [0.0, 0.0]], 5.0),
+    # equal inputs: exactly 0
+    ([[0.5, -0.25], [2.0, 8.0]], [[0.5, -0.25], [2.0, 8.0]], 0.0),
+]
+
+
+@pytest.mark.parametrize("y,y_ref,want", ERROR_HAND_CASES)
+def test_rel_fro_error_hand_cases(y, y_ref, want):
+    got = ons.rel_fro_error(np.array(y), np.array(y_ref))
+    assert abs(got - want) <= 1e-15 * max(1.0, want), (got, want)
+
+
+def test_rel_fro_error_properties():
+    rng = np.random.default_rng(7)
+    y_ref = rng.standard_normal((13, 21))
+    d = rng.standard_normal((13, 21))
+    d *= 1e-3 * np.linalg.norm(y_ref) / np.linalg.norm(d)
+    # a perturbation of relative size 1e-3 measures 1e-3, in either sign
+    assert abs(ons.rel_fro_error(y_ref + d, y_ref) - 1e-3) < 1e-15
+    assert abs(ons.rel_fro_error(y_ref - d, y_ref) - 1e-3) < 1e-15
+    # invariant to a common scale of both arguments
+    assert abs(ons.rel_fro_error(4.0 * (y_ref + d), 4.0 * y_ref) - 1e-3) < 1e-15
+    # float32 and bfloat16-sized inputs are measured in float64
+    y32 = (y_ref + d).astype(np.float32)
+    assert abs(ons.rel_fro_error(y32, y_ref) - np.linalg.norm(y32.astype(np.float64) - y_ref)
+               / np.linalg.norm(y_ref)) < 1e-15
