@@ -264,10 +264,17 @@ int ns_check_status(ns_plan_t* plan, void* stream);
  * Allocates nothing (no cudaMalloc, no cudaFree). Returns NS_ERR_WORKSPACE if
  * the plan needs more than NS_FIXED_WS_BYTES (see ns_plan_workspace_bytes).
  * The array exists once per GPU that loads the library and is held until the
- * process exits. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. Every call shares the array, so calls that
- * overlap on the GPU (e.g. on two streams) race. */
+ * process exits. When it is reserved depends on CUDA's module loading: under
+ * lazy loading (the default) the first call on a device, which looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current,
+ * loads the module holding it and so reserves the NS_FIXED_WS_BYTES then --
+ * that first call can fail with NS_ERR_CUDA if the GPU is already full, so
+ * make it at start-up (and before any stream capture); under eager loading
+ * (CUDA_MODULE_LOADING=EAGER) every process that loads the library holds the
+ * array from the start, whether or not it calls this function. Every call
+ * shares the array and finds the previous call's contents there (the kernels
+ * write every byte they read first), so calls that overlap on the GPU (e.g.
+ * on two streams) race. */
 #define NS_FIXED_WS_BYTES (64ull << 20)
 int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, void* const* out, int n,
                                       void* stream);

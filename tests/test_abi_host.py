@@ -41,6 +41,11 @@ def test_header_constants_match_the_binding():
     assert len(consts) >= 17
     for k, v in consts.items():
         assert getattr(_lib, k) == v, k
+    # sizes the header defines as (value << shift)
+    defs = re.findall(r"#define\s+(NS_[A-Z0-9_]+)\s+\((\d+)ull\s*<<\s*(\d+)\)", hdr)
+    assert [k for k, _, _ in defs] == ["NS_FIXED_WS_BYTES"]
+    for k, v, sh in defs:
+        assert getattr(nsg, k) == int(v) << int(sh), k
 
 
 def test_ns_cost_hand_values_and_oracle():

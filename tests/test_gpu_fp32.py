@@ -19,17 +19,14 @@ nsg = pytest.importorskip("newton_schulz_shape_gb300")
 FP32_TOL = 1e-3
 
 
-def run_f32(shapes, ts, steps=workloads.STEPS, ridge=0.0, fixed_ws=False):
+def run_f32(shapes, ts, steps=workloads.STEPS, ridge=0.0):
     dev = torch.device("cuda:0")
     ins = [t.to(dev) for t in ts]
     outs = [torch.full(t.shape, float("nan"), dtype=torch.float32, device=dev) for t in ins]
     plan = nsg.ns_plan_create(shapes, steps=steps, eps=workloads.EPS, gram_mode=nsg.NS_FP32_GRAM, ridge=ridge, S=1)
     assert plan.out_bytes == 4
-    if fixed_ws:
-        nsg.ns_orthogonalize_batched_fixed_ws(plan, ins, outs)
-    else:
-        ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
-        nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
     rc = nsg.ns_check_status(plan)
     assert rc == nsg.NS_OK, nsg.ns_status_string(rc)
     return outs
