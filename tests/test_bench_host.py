@@ -58,3 +58,17 @@ def test_executed_never_below_useful_for_full_tiles():
         fl = bench.flops_by_kind([shape], 5)
         ex = bench.executed_flops_by_kind([shape], 5)
         assert ex["bx"] > fl["bx"]
+
+
+def test_reference_arm_splits_the_workload_once():
+    # the reference arm's timed steps together run every matrix exactly once
+    w = bench.get_workload("gpt")
+    for k in (1, 3, 20, 95, 96, 200):
+        groups = bench.split_by_flops(w, k)
+        assert len(groups) == min(k, len(w.shapes))
+        assert [i for g in groups for i in g] == list(range(len(w.shapes)))
+
+
+def test_blas_threads_reported():
+    n = bench.blas_threads()
+    assert n is None or n >= 1

@@ -163,3 +163,32 @@ def test_fp32_auto_matches_the_mode_of_each_bucket():
         alone = run_mode([s], [t], mode)[0]
         assert torch.equal(o.cpu(), alone.cpu()), s
         assert rel_err(o, oracle(t)) <= FP32_TOL, s
+
+
+# Full sweep sizes (the size/aspect sweep's points, whole batches as the
+# sweep runs them): every matrix finite with ||Y||_F / sqrt(m) in the 5-step
+# band, the first of the batch against the oracle at the fp32 bar.
+SWEEP_BATCH = {(m, a): bt for m, a, bt in workloads.sweep_points()}
+
+
+@pytest.mark.parametrize("m,aspect,mode", [(4096, 1, nsg.NS_FP32_GRAM), (4096, 4, nsg.NS_FP32_AUTO),
+                                           (8192, 1, nsg.NS_FP32_GRAM), (2048, 8, nsg.NS_FP32_AUTO)])
+def test_fp32_sweep_points_full_size(m, aspect, mode):
+    w = workloads.sweep_shapes(m, aspect, SWEEP_BATCH[(m, aspect)])
+    ts = workloads.gen_tensors(w, indices=[0])
+    dev = torch.device("cuda:0")
+    # the batch's other matrices come from the same generator, on the GPU side only
+    ins = [ts[0].to(dev)] + [workloads.gen_tensor(s, w.sigma, w.seed, i).to(dev)
+                             for i, s in enumerate(w.shapes) if i > 0]
+    outs = [torch.full(t.shape, float("nan"), dtype=torch.float32, device=dev) for t in ins]
+    plan = nsg.ns_plan_create(w.shapes, steps=workloads.STEPS, eps=workloads.EPS, gram_mode=mode, S=1)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    del ws
+    for i, o in enumerate(outs):
+        assert torch.isfinite(o).all(), i
+        f = float(torch.linalg.vector_norm(o.double())) / m ** 0.5
+        assert 0.5 < f < 1.2, (i, f)
+    err = rel_err(outs[0], oracle(ts[0]))
+    assert err <= FP32_TOL, (m, aspect, err)

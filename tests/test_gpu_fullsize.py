@@ -127,19 +127,23 @@ def test_sweep_8192_square():
     run_pipeline(w, sample=[0])
 
 
-def test_max_sweep_size_closed_form():
+@pytest.mark.parametrize("mode", ["bf16", "fp32_auto"])
+def test_max_sweep_size_closed_form(mode):
     # the sweep's largest matrix, 8192 x 65536 (1 GiB of bf16), wide and tall
     # in one batch, against the closed form NS_k(X)_i = g_i X_i of an input
     # with orthogonal rows. Checked per matrix (relative Frobenius error, the
-    # bf16 bar) and per 128 x 256 output tile, so that one wrong tile anywhere
-    # in the 2^29 elements fails.
+    # policy's bar) and per 128 x 256 output tile, so that one wrong tile
+    # anywhere in the 2^29 elements fails. fp32_auto runs these shapes in Gram
+    # space (n = 8m).
+    gram_mode, odt, tol, tile_tol = {"bf16": (nsg.NS_BF16, torch.bfloat16, BF16_TOL, 0.1),
+                                     "fp32_auto": (nsg.NS_FP32_AUTO, torch.float32, 1e-3, 1e-2)}[mode]
     dev = torch.device("cuda:0")
     m, blocks = 8192, 8
     x, r, d = workloads.gen_hadamard_rows(m, blocks, seed=5807, device="cuda")
     shapes = [(m, m * blocks), (m * blocks, m)]
     ins = [x, x.t().contiguous()]
-    outs = [torch.empty_like(t) for t in ins]
-    plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=1)
+    outs = [torch.empty(t.shape, dtype=odt, device=dev) for t in ins]
+    plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, gram_mode=gram_mode, S=1)
     ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
     nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
     assert nsg.ns_check_status(plan) == nsg.NS_OK
@@ -161,5 +165,5 @@ def test_max_sweep_size_closed_form():
             worst_tile = max(worst_tile, float((dt / wt).sqrt().max()))
             del want, diff
         err = math.sqrt(num / den)
-        assert err <= BF16_TOL, (tall, err)
-        assert worst_tile <= 0.1, (tall, worst_tile)
+        assert err <= tol, (mode, tall, err)
+        assert worst_tile <= tile_tol, (mode, tall, worst_tile)
