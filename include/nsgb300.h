@@ -176,6 +176,26 @@ int ns_owner_gather_meta(const ns_plan_t* plan, int rho, int64_t* send_sizes, in
 int ns_owner_scatter_meta(const ns_plan_t* plan, int rho, int64_t* send_sizes, int64_t* recv_sizes,
                           int64_t* recv_offsets);
 
+/* [LSA] route_to_ns_home / route_from_ns_home as one all_to_allv of row
+ * shards, seen from rank rho (row-shard and two-stage plans; flat plans use
+ * ns_owner_gather_meta, NS_ERR_ARG here). Every rank holds a piece of
+ * numel/S elements of every participating tensor.
+ *   send_counts[h], send_displs[h]: elements rho sends to home h and their
+ *     offset in rho's send buffer, which holds, home by home in rank order,
+ *     rho's pieces of the tensors homed on h in index order;
+ *   recv_counts[s], recv_displs[s]: elements rho receives from rank s and
+ *     their offset in rho's receive buffer (source by source in rank order,
+ *     each segment the pieces of the tensors homed on rho in index order);
+ *   send_pos[i]: offset of rho's piece of tensor i in its send buffer (-1 if
+ *     tensor i does not participate);
+ *   recv_pos[i*S + s]: offset of rank s's piece of tensor i in rho's receive
+ *     buffer (-1 unless rho is tensor i's home).
+ * The reverse exchange (route_from_ns_home) swaps the send and receive
+ * sides. Arrays of S (counts, displs), n_tensors (send_pos) and n_tensors*S
+ * (recv_pos) entries; any pointer may be NULL. Host only. */
+int ns_plan_rank_splits(const ns_plan_t* plan, int rho, int64_t* send_counts, int64_t* send_displs,
+                        int64_t* recv_counts, int64_t* recv_displs, int64_t* send_pos, int64_t* recv_pos);
+
 const char* ns_status_string(int status);
 
 /* ----------------------------------------------------------------- device */

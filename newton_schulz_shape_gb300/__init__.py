@@ -123,6 +123,17 @@ class NsPlan:
         check(lib.ns_owner_scatter_meta(self._h, rho, send, recv, roff), "ns_owner_scatter_meta")
         return list(send), list(recv), [list(roff[i * S:(i + 1) * S]) for i in range(n)]
 
+    def rank_splits(self, rho: int):
+        """route_to_ns_home as one all_to_allv seen from rank rho:
+        (send_counts, send_displs, recv_counts, recv_displs, send_pos, recv_pos)
+        with recv_pos[i][s] the offset of rank s's piece of tensor i."""
+        n, S = self.n_tensors, self.S
+        sc, sd, rc, rd = [(ctypes.c_int64 * S)() for _ in range(4)]
+        sp, rp = (ctypes.c_int64 * max(1, n))(), (ctypes.c_int64 * max(1, n * S))()
+        check(lib.ns_plan_rank_splits(self._h, rho, sc, sd, rc, rd, sp, rp), "ns_plan_rank_splits")
+        return (list(sc), list(sd), list(rc), list(rd), list(sp[:n]),
+                [list(rp[i * S:(i + 1) * S]) for i in range(n)])
+
     def __del__(self):
         h = getattr(self, "_h", None)
         if h:

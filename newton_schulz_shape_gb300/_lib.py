@@ -54,6 +54,7 @@ _SIGS = {
                                                 ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                                 ctypes.c_float, ctypes.c_int, ctypes.c_float, _i32p,
                                                 ctypes.POINTER(_planp)]),
+    "ns_plan_rank_splits": (ctypes.c_int, [_planp, ctypes.c_int, _i64p, _i64p, _i64p, _i64p, _i64p, _i64p]),
     "ns_plan_destroy": (ctypes.c_int, [_planp]),
     "ns_plan_info": (ctypes.c_int, [_planp, _i64p]),
     "ns_plan_homes": (ctypes.c_int, [_planp, _i32p]),

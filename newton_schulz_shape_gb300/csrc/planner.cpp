@@ -645,6 +645,47 @@ int ns_owner_scatter_meta(const ns_plan_t* plan, int rho, int64_t* send_sizes, i
   return nsplan::scatter_meta(plan->p, rho, send_sizes, recv_sizes, recv_offsets);
 }
 
+// [LSA] route_to_ns_home as one all_to_allv, seen from rank rho (row-shard
+// and two-stage plans). rho's send buffer holds, for each home h in rank
+// order, rho's pieces of the tensors homed on h in index order; its receive
+// buffer holds, for each source s in rank order, s's pieces of the tensors
+// homed on rho in index order. route_from_ns_home is the same exchange with
+// the send and receive sides swapped.
+int ns_plan_rank_splits(const ns_plan_t* plan, int rho, int64_t* send_counts, int64_t* send_displs,
+                        int64_t* recv_counts, int64_t* recv_displs, int64_t* send_pos, int64_t* recv_pos) {
+  if (!plan || plan->p.layout == NS_LAYOUT_FLAT || rho < 0 || rho >= plan->p.S) return NS_ERR_ARG;
+  const nsplan::Plan& p = plan->p;
+  const int S = p.S;
+  const size_t n = p.t.size();
+  std::vector<int64_t> sc(S, 0), sd(S, 0);
+  int64_t mine = 0;  // elements of one source's pieces of the tensors homed on rho
+  for (size_t i = 0; i < n; ++i) {
+    const nsplan::Tensor& t = p.t[i];
+    if (!t.participating) continue;
+    sc[t.home] += t.shard_len;
+    if (t.home == rho) mine += t.shard_len;
+  }
+  for (int h = 1; h < S; ++h) sd[h] = sd[h - 1] + sc[h - 1];
+  std::vector<int64_t> fill(sd);
+  int64_t in_mine = 0;  // offset of a tensor's piece inside one source's segment
+  for (size_t i = 0; i < n; ++i) {
+    const nsplan::Tensor& t = p.t[i];
+    const bool part = t.participating;
+    if (send_pos) send_pos[i] = part ? fill[t.home] : -1;
+    if (part) fill[t.home] += t.shard_len;
+    for (int src = 0; src < S; ++src)
+      if (recv_pos) recv_pos[i * S + src] = (part && t.home == rho) ? src * mine + in_mine : -1;
+    if (part && t.home == rho) in_mine += t.shard_len;
+  }
+  for (int r = 0; r < S; ++r) {
+    if (send_counts) send_counts[r] = sc[r];
+    if (send_displs) send_displs[r] = sd[r];
+    if (recv_counts) recv_counts[r] = mine;
+    if (recv_displs) recv_displs[r] = r * mine;
+  }
+  return NS_OK;
+}
+
 const char* ns_status_string(int status) {
   switch (status) {
     case NS_OK: return "ok";

@@ -300,3 +300,52 @@ def test_pipeline_with_nothing_participating():
     with pytest.raises(nsg.NsError) as e:
         nsg.ns_pipeline_create(nsg.ns_plan_create([(8, 8)], S=1), 0)
     assert e.value.code == nsg.NS_ERR_ARG
+
+
+@pytest.mark.parametrize("kind,S", [("row", 1), ("row", 3), ("row", 8), ("row_dim1", 4), ("two_stage", 4)])
+def test_rank_splits_simulated_all_to_allv(kind, S):
+    # every rank's view of the exchange, simulated with numpy: the pieces each
+    # home receives are exactly the pieces the sources hold
+    if kind == "row":
+        shapes = workloads.gen_random_shapes(17, 300 + S, 120, S)
+        plan = nsg.ns_plan_create(shapes, S=S, shard_dim=0)
+    elif kind == "row_dim1":
+        shapes = [(5, 12, 7), (3, 24, 4), (2, 36, 8), (6, 12, 4), (1, 4)]
+        plan = nsg.ns_plan_create(shapes, S=S, shard_dim=1)
+    else:
+        shapes = [(48, 24), (24, 48, 4), (96, 16), (24, 8, 8), (48, 12)]
+        plan = nsg.ns_plan_create_two_stage(shapes, [1, 1, 0, 2, 1], 2, 2)
+    homes = plan.homes()
+    _, _, rank_sizes = plan.home_layout()
+    n = len(shapes)
+    piece = [int(np.prod(s)) // S for s in shapes]
+    roff = np.concatenate([[0], np.cumsum(piece)])
+    # rank r's buffer: a distinct value per (rank, element)
+    bufs = [np.arange(rank_sizes[r]) + 10**6 * (r + 1) for r in range(S)]
+    views = [plan.rank_splits(r) for r in range(S)]
+    sends = []
+    for r, (sc, sd, rc, rd, sp, rp) in enumerate(views):
+        assert sum(sc) == rank_sizes[r] and sd == list(np.concatenate([[0], np.cumsum(sc)[:-1]]))
+        snd = np.full(sum(sc), -1)
+        for i in range(n):
+            snd[sp[i]:sp[i] + piece[i]] = bufs[r][roff[i]:roff[i + 1]]
+        assert (snd >= 0).all()                      # the pieces tile the send buffer
+        sends.append(snd)
+    for r, (sc, sd, rc, rd, sp, rp) in enumerate(views):
+        # all_to_allv: segment s of r's receive buffer is what s sends to r
+        recv = np.concatenate([sends[s][views[s][1][r]:views[s][1][r] + views[s][0][r]] for s in range(S)])
+        assert list(rc) == [views[s][0][r] for s in range(S)]
+        for i in range(n):
+            for s in range(S):
+                if homes[i] == r:
+                    got = recv[rp[i][s]:rp[i][s] + piece[i]]
+                    assert np.array_equal(got, bufs[s][roff[i]:roff[i + 1]]), (kind, i, s, r)
+                else:
+                    assert rp[i][s] == -1
+
+
+def test_rank_splits_rejects_flat_plans():
+    plan = nsg.ns_plan_create_flat([(6, 4), (4, 4)], [0, 24], 40, S=2)
+    with pytest.raises(nsg.NsError) as e:
+        plan.rank_splits(0)
+    assert e.value.code == nsg.NS_ERR_ARG

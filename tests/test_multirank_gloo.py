@@ -2,10 +2,12 @@
 
 * Every rank builds the plan independently through the C ABI and gets the
   same homes and home layout (a real exchange needs all ranks to agree).
-* The plan's split sizes drive a real all_to_all of the row shards
-  (layer_sharded_a2a, route_to_ns_home on a 2-rank group): each home's
-  reconstructed buffer equals the oracle's, bit for bit; the reverse
-  all_to_all (route_from_ns_home) gives every rank its shards back.
+* The plan's all_to_allv splits and piece positions (ns_plan_rank_splits)
+  drive a real all_to_all of the row shards (layer_sharded_a2a,
+  route_to_ns_home on a 2-rank group): each home's reconstructed buffer
+  equals the oracle's, bit for bit; the reverse all_to_all
+  (route_from_ns_home, the same splits with the sides swapped) gives every
+  rank its shards back.
 * The bench's max-over-ranks timing and whole-job value.
 """
 
@@ -53,41 +55,36 @@ def _worker(rank, port, errfile):
         ts = [t.view(torch.int16).numpy().astype(np.int32) for t in workloads.gen_tensors(w)]
         ranks = orr.make_rank_buffers(ts, WORLD, 0)
         local = torch.from_numpy(ranks[rank].copy())
-        # send split to home h: this rank's shards of the params homed on h
+        # the all_to_allv splits and piece positions come from the plan
+        send_counts, send_displs, recv_counts, recv_displs, send_pos, recv_pos = plan.rank_splits(rank)
         shard = [int(np.prod(s)) // WORLD for s in w.shapes]
-        send_idx = [[i for i in range(len(w.shapes)) if homes[i] == h] for h in range(WORLD)]
         off = np.concatenate([[0], np.cumsum(shard)])
-        send = torch.cat([torch.cat([local[off[i]:off[i + 1]] for i in send_idx[h]]) if send_idx[h]
-                          else torch.zeros(0, dtype=torch.int32) for h in range(WORLD)])
-        in_splits = [sum(shard[i] for i in send_idx[rank])] * WORLD
-        out_splits = [sum(shard[i] for i in send_idx[h]) for h in range(WORLD)]
-        recv = torch.zeros(sum(in_splits), dtype=torch.int32)
-        dist.all_to_all_single(recv, send, in_splits, out_splits)
-        # reconstruct the complete params homed here: shards in rank order
-        parts, pos = {i: [] for i in send_idx[rank]}, 0
-        for src in range(WORLD):
-            for i in send_idx[rank]:
-                parts[i].append(recv[pos:pos + shard[i]].numpy())
-                pos += shard[i]
-        home = np.concatenate([np.concatenate([p.reshape(w.shapes[i][0] // WORLD, -1) for p in parts[i]],
-                                              axis=0).reshape(-1) for i in send_idx[rank]]) \
-            if send_idx[rank] else np.zeros(0, np.int32)
+        send = torch.zeros(sum(send_counts), dtype=torch.int32)
+        for i in range(len(w.shapes)):
+            send[send_pos[i]:send_pos[i] + shard[i]] = local[off[i]:off[i + 1]]
+        recv = torch.zeros(sum(recv_counts), dtype=torch.int32)
+        dist.all_to_all_single(recv, send, recv_counts, send_counts)
+        # reconstruct the complete params homed here: pieces in rank order
+        mine = [i for i in range(len(w.shapes)) if homes[i] == rank]
+        home = np.concatenate([np.concatenate([recv[recv_pos[i][src]:recv_pos[i][src] + shard[i]].numpy()
+                                               .reshape(w.shapes[i][0] // WORLD, -1) for src in range(WORLD)],
+                                              axis=0).reshape(-1) for i in mine]) \
+            if mine else np.zeros(0, np.int32)
         want = orr.route_to_ns_home(ranks, w.shapes, dict(enumerate(homes)), WORLD, 0)[rank]
         assert np.array_equal(home, want)
         assert home.size == hs[rank]
 
-        # reverse exchange: every rank gets its shard of every param back
-        back_send = torch.cat([torch.from_numpy(home[ho[i]:ho[i] + int(np.prod(w.shapes[i]))].copy())
-                               .reshape(WORLD, -1)[dst] for dst in range(WORLD) for i in send_idx[rank]]) \
-            if send_idx[rank] else torch.zeros(0, dtype=torch.int32)
-        back = torch.zeros(local.numel(), dtype=torch.int32)
-        dist.all_to_all_single(back, back_send, out_splits, in_splits)
-        got, pos = {}, 0
-        for h in range(WORLD):
-            for i in send_idx[h]:
-                got[i] = back[pos:pos + shard[i]]
-                pos += shard[i]
-        assert torch.equal(torch.cat([got[i] for i in range(len(w.shapes))]), local)
+        # reverse exchange (route_from_ns_home): the same splits with the
+        # sides swapped; every rank gets its shard of every param back
+        back_send = torch.zeros(sum(recv_counts), dtype=torch.int32)
+        for i in mine:
+            full = torch.from_numpy(home[ho[i]:ho[i] + int(np.prod(w.shapes[i]))].copy()).reshape(WORLD, -1)
+            for dst in range(WORLD):
+                back_send[recv_pos[i][dst]:recv_pos[i][dst] + shard[i]] = full[dst]
+        back_recv = torch.zeros(sum(send_counts), dtype=torch.int32)
+        dist.all_to_all_single(back_recv, back_send, send_counts, recv_counts)
+        back = torch.cat([back_recv[send_pos[i]:send_pos[i] + shard[i]] for i in range(len(w.shapes))])
+        assert torch.equal(back, local)
 
         # bench aggregation: max over ranks, whole-job value
         t = bench.max_over_ranks(10.0 + rank, WORLD)
