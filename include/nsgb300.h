@@ -299,6 +299,28 @@ int ns_check_status(ns_plan_t* plan, void* stream);
 int ns_orthogonalize_batched_fixed_ws(ns_plan_t* plan, const void* const* in, void* const* out, int n,
                                       void* stream);
 
+/* ---------------------------------------------------------- test support
+ * No counterpart on the pages: hooks with which tests drive the library's
+ * device-side error paths without faulting or hanging the GPU. */
+
+/* Arms the next bf16 GEMM launch of this process (any phase, any thread) to
+ * stall: its TMA producer issues no copy, so its MMA issuer's first wait for
+ * operands cannot complete; every wait of that launch is bounded by
+ * wait_limit_ns (1e5 .. 1e10 ns, else NS_ERR_ARG), after which the kernel
+ * records a timeout in the device status word and unwinds (nothing is in
+ * flight: no copy or MMA was issued). The call that contains the launch
+ * returns normally but its results are garbage; ns_check_status then reports
+ * NS_ERR_TIMEOUT, and later calls run normally. One-shot. */
+int ns_test_stall_next_gemm(uint64_t wait_limit_ns);
+
+/* Sets the home index of tensor `tensor` in the plan's routing table (and in
+ * every device copy already uploaded) to `home`, which may be out of range:
+ * pack and unpack then refuse that tensor's entry (its data is not moved),
+ * record the refusal in the device status word, and ns_check_status reports
+ * NS_ERR_DEVICE_CHECK. Restore the plan's own home to undo. NS_ERR_ARG if
+ * the tensor has no routing entry. Synchronous (cudaMemcpy). */
+int ns_test_set_route_home(ns_plan_t* plan, int tensor, int home);
+
 /* ------------------------------------------------------------ measurement
  * Not part of the pages' interface: support for measuring the kernels above.
  * Kernel kinds: 0 = Gram (X X^T), 1 = A*A with the b*A + c*A^2 epilogue,

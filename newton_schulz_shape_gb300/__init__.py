@@ -296,3 +296,15 @@ def ns_pipeline_run(pipe: NsPipeline, rank_in, home_in, home_out, rank_out, work
                               ptr_array([_addr(t) for t in home_in]), ptr_array([_addr(t) for t in home_out]),
                               ptr_array([_addr(t) for t in rank_out]), _addr(workspace), nbytes, _stream(stream)),
           "ns_pipeline_run")
+
+
+def ns_test_stall_next_gemm(wait_limit_ns: int) -> None:
+    """Test support: the next bf16 GEMM launch stalls and its bounded waits run
+    out after wait_limit_ns; ns_check_status then reports NS_ERR_TIMEOUT."""
+    check(lib.ns_test_stall_next_gemm(int(wait_limit_ns)), "ns_test_stall_next_gemm")
+
+
+def ns_test_set_route_home(plan: NsPlan, tensor: int, home: int) -> None:
+    """Test support: overwrite a tensor's home in the plan's routing table
+    (out-of-range values make pack/unpack refuse it: NS_ERR_DEVICE_CHECK)."""
+    check(lib.ns_test_set_route_home(plan.handle, tensor, home), "ns_test_set_route_home")

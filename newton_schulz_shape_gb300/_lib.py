@@ -55,6 +55,8 @@ _SIGS = {
                                                 ctypes.c_float, ctypes.c_int, ctypes.c_float, _i32p,
                                                 ctypes.POINTER(_planp)]),
     "ns_plan_rank_splits": (ctypes.c_int, [_planp, ctypes.c_int, _i64p, _i64p, _i64p, _i64p, _i64p, _i64p]),
+    "ns_test_stall_next_gemm": (ctypes.c_int, [ctypes.c_uint64]),
+    "ns_test_set_route_home": (ctypes.c_int, [_planp, ctypes.c_int, ctypes.c_int]),
     "ns_plan_destroy": (ctypes.c_int, [_planp]),
     "ns_plan_info": (ctypes.c_int, [_planp, _i64p]),
     "ns_plan_homes": (ctypes.c_int, [_planp, _i32p]),

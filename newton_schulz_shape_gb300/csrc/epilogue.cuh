@@ -105,7 +105,8 @@ __device__ __forceinline__ uint32_t epi_swz(int y, int u) {
 // release(acc): signal that TMEM accumulator `acc` may be overwritten.
 template <int PHASE, bool FINAL, typename P, typename Dec, typename Release>
 __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const Release& release, uint32_t tmem_base,
-                                              int lg, int lane, long long t0, long long tstride, uint64_t* tfull,
+                                              int lg, int lane, long long t0, long long tstride, uint64_t lim,
+                                              uint64_t* tfull,
                                               uint8_t* ring, uint64_t* rfull, volatile int* abort_flag) {
   constexpr bool SYRK = PHASE != PH_BX;
   constexpr bool AUX = PHASE != PH_GRAM;
@@ -133,7 +134,7 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
     const EpiTile e = epi_tile<PHASE>(p, dec, t, lg);
     const GemmBucket& B = p.bk[e.b];
     // waits are warp-uniform: a lane that timed out stops the whole warp
-    const bool got = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
+    const bool got = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status, lim);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
@@ -153,7 +154,7 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
       uint8_t* slot = ring + s * EPI_SLOT_BYTES;
       const int cg = e.tn * GEMM_BN + ci * 32;
       if (AUX) {
-        const bool got = mbar_wait(&rfull[s], static_cast<uint32_t>((g / EPI_SLOTS) & 1), abort_flag, p.status);
+        const bool got = mbar_wait(&rfull[s], static_cast<uint32_t>((g / EPI_SLOTS) & 1), abort_flag, p.status, lim);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;

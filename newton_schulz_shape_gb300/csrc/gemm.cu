@@ -136,17 +136,18 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
   // everything above is set-up; the data path starts after the predecessor
   griddep_wait();
   griddep_launch_dependents();
+  const uint64_t lim = p.wait_ns ? p.wait_ns : NS_WAIT_LIMIT_NS;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
-    for (long long t = t0; t < p.total_tiles; t += tstride) {
+    for (long long t = p.stall ? p.total_tiles : t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
       decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
         uint8_t* a_dst = sA + stage * A_BYTES;
         uint8_t* b_dst = sB + stage * B_BYTES;
@@ -180,11 +181,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       int b, mat, tm, tn;
       decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
-      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, lim)) goto mma_done;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto mma_done;
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       decode_tile<PHASE>(p, t, b, mat, tm, tn);
     };
     auto release = [&](uint32_t a) { mbar_arrive(&tempty[a]); };
-    epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, tfull,
+    epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, lim, tfull,
                                 ring + lg * EPI_SLOTS * EPI_SLOT_BYTES, rfull + lg * EPI_SLOTS, abort_flag);
   }
 

@@ -142,17 +142,18 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
   // everything above is set-up; the data path starts after the predecessor
   griddep_wait();
   griddep_launch_dependents();
+  const uint64_t lim = p.wait_ns ? p.wait_ns : NS_WAIT_LIMIT_NS;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
-    for (long long t = t0; t < p.total_tiles; t += tstride) {
+    for (long long t = p.stall ? p.total_tiles : t0; t < p.total_tiles; t += tstride) {
       int b, mat, tm, tn;
       decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) goto producer_done;
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         const uint32_t full_l = map_to_rank(&full[stage], 0);
         if (leader) mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
         tma_load_3d_pair(sA + stage * A_BYTES, &p.tma[b], full_l, kb * BK, tm * BM, mat);
@@ -185,11 +186,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       int b, mat, tm, tn;
       decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
-      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) goto mma_done;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, lim)) goto mma_done;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto mma_done;
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
     };
     // the leader's MMA waits for all 8 epilogue warps of the pair
     auto release = [&](uint32_t a) { mbar_arrive_cluster(map_to_rank(&tempty[a], 0)); };
-    epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, tfull,
+    epilogue_warp<PHASE, FINAL>(p, dec, release, tmem_base, lg, lane, t0, tstride, lim, tfull,
                                 ring + lg * EPI_SLOTS * EPI_SLOT_BYTES, rfull + lg * EPI_SLOTS, abort_flag);
   }
 

@@ -55,6 +55,12 @@ struct GemmParamsT {
   int nb;
   float alpha, beta, gamma;  // a, b, c of the quintic step
   int reverse;               // walk the tiles last to first (serpentine order across launches)
+  // Test support: wait_ns (0 = NS_WAIT_LIMIT_NS) bounds every mbarrier wait of
+  // the launch; stall != 0 makes the TMA producer issue no copy at all, so the
+  // MMA issuer's first wait for operands runs out after wait_ns and the
+  // kernel unwinds with NS_DEV_TIMEOUT recorded (nothing is in flight then).
+  unsigned long long wait_ns;
+  int stall;
   int out_ranks;             // final-store launches: out_tab holds rank-buffer offsets
   int S;                     // ranks of rank_ptr (out_ranks)
   void* rank_ptr[ROUTE_MAX_RANKS];

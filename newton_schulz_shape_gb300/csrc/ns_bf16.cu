@@ -174,6 +174,10 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
   int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl), first_step);
   if (rc != NS_OK) return rc;
   gp.reverse = reverse ? 1 : 0;
+  if (const unsigned long long ns = take_gemm_stall()) {
+    gp.stall = 1;
+    gp.wait_ns = ns;
+  }
   return counted(phase, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair(phase, gp, nsm, st) : nsk::launch_gemm(phase, gp, nsm, st);
          }) == cudaSuccess
@@ -190,6 +194,10 @@ int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, 
   int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step, rank_out);
   gp.reverse = reverse ? 1 : 0;
   if (rc != NS_OK) return rc;
+  if (const unsigned long long ns = take_gemm_stall()) {
+    gp.stall = 1;
+    gp.wait_ns = ns;
+  }
   return counted(K_BX_FINAL, st, [&] {
            return cl == 3 ? nsk::launch_gemm_pair_final(gp, nsm, st) : nsk::launch_gemm_final(gp, nsm, st);
          }) == cudaSuccess

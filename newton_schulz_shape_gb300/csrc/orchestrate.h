@@ -25,6 +25,9 @@ using nsplan::Tensor;
 int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out);
 // GEMM tiling forced by ns_set_gemm_cluster (0: automatic).
 int gemm_cluster_override();
+// Test support: the wait limit armed by ns_test_stall_next_gemm (0 if none),
+// cleared by this call; the launch that takes it stalls.
+unsigned long long take_gemm_stall();
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

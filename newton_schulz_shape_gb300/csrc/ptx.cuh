@@ -60,10 +60,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed. Returns
-// false (after flagging) if the CTA's abort flag is up or the time limit ran
-// out.
+// false (after flagging) if the CTA's abort flag is up or the time limit
+// (limit_ns of %globaltimer time) ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* status) {
+                                          unsigned int* status, uint64_t limit_ns = NS_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -71,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > NS_WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, NS_DEV_TIMEOUT);
       return false;

@@ -96,6 +96,37 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
                plan ? plan->p.out_bytes : 2, static_cast<cudaStream_t>(stream));
 }
 
+int ns_test_set_route_home(ns_plan_t* plan, int tensor, int home) {
+  if (!plan || tensor < 0 || tensor >= static_cast<int>(plan->p.t.size())) return NS_ERR_ARG;
+  Plan& p = plan->p;
+  // the table holds one entry per participating tensor with data, in index order
+  size_t k = 0;
+  bool found = false;
+  for (int i : p.part) {
+    const Tensor& t = p.t[i];
+    if (p.layout != NS_LAYOUT_FLAT ? t.shard_len == 0 : t.numel == 0) continue;
+    if (i == tensor) {
+      found = true;
+      break;
+    }
+    ++k;
+  }
+  if (!found || k >= p.route.size()) return NS_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_route_mu);
+  p.route[k].home = home;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) cur = -1;
+  int rc = NS_OK;
+  for (int d = 0; d < nsplan::kMaxDevices; ++d) {
+    if (!p.d_route[d]) continue;
+    nsk::RouteEntry* dev_e = static_cast<nsk::RouteEntry*>(p.d_route[d]) + k;
+    if (cudaSetDevice(d) != cudaSuccess || cudaMemcpy(&dev_e->home, &home, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      rc = NS_ERR_CUDA;
+  }
+  if (cur >= 0) cudaSetDevice(cur);
+  return rc;
+}
+
 int ns_plan_destroy(ns_plan_t* plan) {
   if (!plan) return NS_OK;
   bool any = false;

@@ -28,6 +28,9 @@ int g_cc_ok[nsplan::kMaxDevices] = {0};  // 0 unknown, 1 sm_103, -1 other
 // set once under g_mu, read without it by every launch's tensor-map encoding
 std::atomic<EncodeTiledFn> g_encode{nullptr};
 int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
+// test support: wait limit (ns) of the next bf16 GEMM launch, which then
+// stalls (0: none armed)
+std::atomic<unsigned long long> g_stall_next{0};
 
 // ----------------------------------------------------------- measurement
 std::mutex g_prof_mu;
@@ -68,6 +71,8 @@ void prof_end(int kind, cudaEvent_t a, cudaEvent_t b) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_pending.push_back({a, b, kind});
 }
+
+unsigned long long take_gemm_stall() { return g_stall_next.exchange(0); }
 
 int gemm_cluster_override() {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -159,6 +164,12 @@ int ns_set_gemm_cluster(int cl) {
   if (cl != 0 && cl != 1 && cl != 3) return NS_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_cl = cl;
+  return NS_OK;
+}
+
+int ns_test_stall_next_gemm(uint64_t wait_limit_ns) {
+  if (wait_limit_ns < 100000ull || wait_limit_ns > 10000000000ull) return NS_ERR_ARG;
+  g_stall_next.store(wait_limit_ns);
   return NS_OK;
 }
 

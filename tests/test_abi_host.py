@@ -349,3 +349,17 @@ def test_rank_splits_rejects_flat_plans():
     with pytest.raises(nsg.NsError) as e:
         plan.rank_splits(0)
     assert e.value.code == nsg.NS_ERR_ARG
+
+
+def test_test_hooks_reject_bad_arguments():
+    for v in (0, 99_999, 10_000_000_001):
+        with pytest.raises(nsg.NsError) as e:
+            nsg.ns_test_stall_next_gemm(v)
+        assert e.value.code == nsg.NS_ERR_ARG
+    plan = nsg.ns_plan_create([(4, 4), (2, 6)], S=2)
+    for t in (-1, 2):
+        with pytest.raises(nsg.NsError) as e:
+            nsg.ns_test_set_route_home(plan, t, 0)
+        assert e.value.code == nsg.NS_ERR_ARG
+    # host-only: no device table uploaded yet, so no CUDA call is made
+    nsg.ns_test_set_route_home(plan, 1, 0)
