@@ -326,7 +326,8 @@ int ns_test_set_route_home(ns_plan_t* plan, int tensor, int home);
  * Kernel kinds: 0 = Gram (X X^T), 1 = A*A with the b*A + c*A^2 epilogue,
  * 2 = B*X with the a*X epilogue, 3 = norm/scale/transpose prologue and
  * output store, 4 = pack/unpack, 5 = the last step's B*X launches, which also
- * store the results (to the caller's tensors or the rank buffers). Launch
+ * store the results (to the caller's tensors or the rank buffers), 6 = the
+ * whole iteration of small matrices, one CTA per matrix. Launch
  * counters are always on. When timing
  * is enabled, every launch is bracketed by two CUDA events recorded on the
  * stream it is launched on; ns_profile_read synchronises those events. */
@@ -342,10 +343,20 @@ int ns_test_set_route_home(ns_plan_t* plan, int tensor, int home);
  * results. */
 int ns_set_gemm_cluster(int cl);
 
+/* Tuning: bf16 shape buckets with m <= 128 and n <= 512 (m, n the short and
+ * long side of the 2-D view) run, when enable = 1 (the default), as one CTA per
+ * matrix that keeps X, A and B in shared memory and the products in TMEM for
+ * the whole iteration: one launch instead of a prologue, 3*steps GEMM
+ * launches and a store. enable = 0 sends them through the GEMM launches like
+ * every other bucket. Same arithmetic (bf16 operands, fp32 accumulation and
+ * epilogues); results agree to rounding, not bit for bit. Other values are
+ * NS_ERR_ARG. Process-wide. */
+int ns_set_small_path(int enable);
+
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */
 int ns_profile_enable(int enable);
 
-/* launches[6] (may be NULL) receives the launch count per kind and gpu_ms[6]
+/* launches[7] (may be NULL) receives the launch count per kind and gpu_ms[7]
  * (may be NULL) the summed event time per kind since the last reset; reset
  * != 0 clears both afterwards. */
 int ns_profile_read(int reset, int64_t* launches, double* gpu_ms);

@@ -242,7 +242,7 @@ def ns_check_status(plan: NsPlan = None, stream=None) -> int:
     return lib.ns_check_status(plan.handle if plan is not None else None, _stream(stream))
 
 
-KERNEL_KINDS = ("gram", "a2b", "bx", "prologue_store", "pack_unpack", "bx_final")
+KERNEL_KINDS = ("gram", "a2b", "bx", "prologue_store", "pack_unpack", "bx_final", "small")
 
 
 def ns_profile_enable(enable: bool = True) -> None:
@@ -263,6 +263,12 @@ def ns_set_gemm_cluster(cl: int) -> None:
     every bucket has an even number of 128-row tile rows), 1 single CTA,
     3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")
+
+
+def ns_set_small_path(enable: bool) -> None:
+    """bf16 buckets with m <= 128 and n <= 512: one CTA per matrix for the whole
+    iteration (True, the default) or the GEMM launches (False)."""
+    check(lib.ns_set_small_path(1 if enable else 0), "ns_set_small_path")
 
 
 class NsPipeline:

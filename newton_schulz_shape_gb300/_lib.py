@@ -78,6 +78,7 @@ _SIGS = {
     "ns_pipeline_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "ns_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "ns_set_gemm_cluster": (ctypes.c_int, [ctypes.c_int]),
+    "ns_set_small_path": (ctypes.c_int, [ctypes.c_int]),
     "ns_profile_read": (ctypes.c_int, [ctypes.c_int, _i64p, ctypes.POINTER(ctypes.c_double)]),
 }
 

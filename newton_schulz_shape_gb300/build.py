@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnsgb300.so")
 SOURCES = ["planner.cpp", "api.cu", "runtime.cu", "route.cu", "ns_bf16.cu", "ns_fp32.cu", "pipeline.cu",
-           "gemm.cu", "gemm2sm.cu", "gemm32.cu", "prologue.cu", "pack.cu", "noalloc.cu"]
+           "gemm.cu", "gemm2sm.cu", "gemm32.cu", "prologue.cu", "pack.cu", "small.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -55,6 +55,8 @@ int ns_orthogonalize_batched(ns_plan_t* plan, const void* const* in, void* const
 
   rc = prologue_bf16(p, in, out, ws, status, st);
   if (rc != NS_OK) return rc;
+  rc = small_bf16(p, in, out, status, st);
+  if (rc != NS_OK) return rc;
   return steps_bf16(p, out, ws, nsm, status, st);
 }
 

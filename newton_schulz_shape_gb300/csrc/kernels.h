@@ -198,6 +198,37 @@ struct PackParams {
   unsigned int* status;
 };
 
+// ------------------------------------------------- small matrices, one CTA each
+// m <= 128 and n <= SMALL_MAX_N: the whole iteration of one matrix runs in
+// one CTA (small.cu), from the input tensor to the result.
+constexpr int SMALL_MAX_M = 128;
+constexpr int SMALL_MAX_N = 512;
+constexpr int SMALL_MAX_MATS = 512;
+
+struct SmallMat {
+  const void* in;      // tensor, row-major rows x cols, bf16 (unused with in_ranks)
+  void* out;           // result, same shape (unused with out_ranks)
+  long long rank_off;  // rank-buffer modes: the tensor's shard offset (elements) in every rank buffer
+  int rows, cols;      // 2-D view (shape[0], prod(shape[1:]))
+  int transposed;      // rows > cols
+  int pad;
+};
+
+struct SmallParams {
+  SmallMat mat[SMALL_MAX_MATS];
+  int count;
+  int n_pad;           // largest n rounded up to 64 over the launch (sizes smem and TMEM)
+  int steps;
+  float a, b, c, eps;
+  int S;               // rank buffers of the rank modes
+  int in_ranks;        // read row j of a tensor from rank j / (rows / S) (row shards along dim 0)
+  int out_ranks;       // write the result rows the same way
+  const void* rank_in[ROUTE_MAX_RANKS];
+  void* rank_out[ROUTE_MAX_RANKS];
+  unsigned int* status;
+};
+static_assert(sizeof(SmallParams) <= 32764, "kernel parameter block too large");
+
 // ----------------------------------------------------------------- launchers
 // 1-SM form: one CTA per 128 x 256 tile. The launchers size the grid from
 // the work items, the SM count and cluster occupancy.
@@ -217,5 +248,6 @@ cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int grid, cudaStream
 cudaError_t launch_ridge32(const Ridge32Params& p, cudaStream_t st);
 cudaError_t launch_prep32(const ProParams& p, cudaStream_t st);
 cudaError_t launch_store32(const ProParams& p, cudaStream_t st);
+cudaError_t launch_small(const SmallParams& p, cudaStream_t st);
 
 }  // namespace nsk

@@ -221,8 +221,11 @@ size_t group_matrices(const Plan& p, size_t b0, size_t b1) {
 int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* ws, unsigned int* status,
                   cudaStream_t st, const void* const* rank_in) {
   // prologue: X~_0 = T or T^T (unscaled, zero padded) with per-block sums of
-  // squares in one pass, then the scales
-  for (const Bucket& b : p.buckets) {
+  // squares in one pass, then the scales (GEMM buckets only: the small ones
+  // load their inputs themselves)
+  const size_t ng = gemm_buckets(p);
+  for (size_t bi = 0; bi < ng; ++bi) {
+    const Bucket& b = p.buckets[bi];
     const BucketPtrs q = bucket_ptrs(b, ws);
     const size_t cnt = b.members.size();
     for (size_t s0 = 0; s0 < cnt; s0 += nsk::PRO_MAX_MATS) {
@@ -269,14 +272,71 @@ int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* 
   return NS_OK;
 }
 
+size_t gemm_buckets(const Plan& p) {
+  if (!small_path_enabled()) return p.buckets.size();
+  size_t n = 0;
+  while (n < p.buckets.size() && !p.buckets[n].small) ++n;
+  return n;
+}
+
 // Whether every bucket group's last B*X launch can store its results itself
-// (its per-matrix table fits the parameter block) and there is a last step.
+// (its per-matrix table fits the parameter block) and there is a last step;
+// small buckets always store their own results.
 bool final_stores_all(const Plan& p) {
+  const size_t ng = gemm_buckets(p);
+  if (ng == 0) return true;
   if (p.steps == 0) return false;
-  for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS)
-    if (group_matrices(p, b0, std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS)) > size_t(nsk::GEMM_MAX_OUT))
+  for (size_t b0 = 0; b0 < ng; b0 += nsk::GEMM_MAX_BUCKETS)
+    if (group_matrices(p, b0, std::min(ng, b0 + nsk::GEMM_MAX_BUCKETS)) > size_t(nsk::GEMM_MAX_OUT))
       return false;
   return true;
+}
+
+int small_bf16(const Plan& p, const void* const* in, void* const* out, unsigned int* status, cudaStream_t st,
+               const void* const* rank_in, void* const* rank_out) {
+  const size_t ng = gemm_buckets(p);
+  if (ng == p.buckets.size()) return NS_OK;
+  static thread_local nsk::SmallParams sp;  // ~21 KB: kept off the stack
+  auto launch = [&]() -> int {
+    if (sp.count == 0) return NS_OK;
+    const int rc = counted(K_SMALL, st, [&] { return nsk::launch_small(sp, st); }) == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+    sp.count = 0;
+    sp.n_pad = 0;
+    return rc;
+  };
+  std::memset(&sp, 0, sizeof(sp));
+  sp.steps = p.steps;
+  sp.a = p.a;
+  sp.b = p.b;
+  sp.c = p.c;
+  sp.eps = p.eps;
+  sp.status = status;
+  sp.S = p.S;
+  sp.in_ranks = rank_in ? 1 : 0;
+  sp.out_ranks = rank_out ? 1 : 0;
+  for (int r = 0; r < p.S && r < nsk::ROUTE_MAX_RANKS; ++r) {
+    sp.rank_in[r] = rank_in ? rank_in[r] : nullptr;
+    sp.rank_out[r] = rank_out ? rank_out[r] : nullptr;
+  }
+  for (size_t bi = ng; bi < p.buckets.size(); ++bi) {
+    const Bucket& b = p.buckets[bi];
+    for (int i : b.members) {
+      const Tensor& t = p.t[i];
+      if (sp.count == nsk::SMALL_MAX_MATS) {
+        const int rc = launch();
+        if (rc != NS_OK) return rc;
+      }
+      nsk::SmallMat& mt = sp.mat[sp.count++];
+      mt.in = rank_in ? nullptr : in[t.ordinal];
+      mt.out = rank_out ? nullptr : out[t.ordinal];
+      mt.rank_off = t.rank_off;
+      mt.rows = static_cast<int>(t.rows);
+      mt.cols = static_cast<int>(t.cols);
+      mt.transposed = t.transposed ? 1 : 0;
+      sp.n_pad = std::max(sp.n_pad, static_cast<int>(b.n_pad));
+    }
+  }
+  return launch();
 }
 
 // bf16 path, part 2: k steps of (Gram, A*A + B, B*X) and the final store.
@@ -289,13 +349,14 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
   // k steps x (Gram, A*A + B, B*X) over all buckets. The last B*X launch of
   // a bucket group writes the results straight to `out` when its per-matrix
   // table fits the parameter block; other groups go through the store kernel.
-  std::vector<char> stored(p.buckets.size(), 0);
+  const size_t ng = gemm_buckets(p);
+  std::vector<char> stored(ng, 0);
   bool cur_is_x0 = true;
   for (int step = 0; step < p.steps; ++step) {
     const bool last = step + 1 == p.steps;
     for (int phase = nsk::PH_GRAM; phase <= nsk::PH_BX; ++phase) {
-      for (size_t b0 = 0; b0 < p.buckets.size(); b0 += nsk::GEMM_MAX_BUCKETS) {
-        const size_t b1 = std::min(p.buckets.size(), b0 + nsk::GEMM_MAX_BUCKETS);
+      for (size_t b0 = 0; b0 < ng; b0 += nsk::GEMM_MAX_BUCKETS) {
+        const size_t b1 = std::min(ng, b0 + nsk::GEMM_MAX_BUCKETS);
         // serpentine order: every other product walks its tiles backwards,
         // starting on the matrices the previous product wrote last (still in L2)
         const bool serp = ((step * 3 + phase) & 1) != 0;
@@ -311,7 +372,7 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
     cur_is_x0 = !cur_is_x0;
   }
   // transpose back and store (buckets not stored by the last B*X launch)
-  for (size_t bi = 0; bi < p.buckets.size(); ++bi) {
+  for (size_t bi = 0; bi < ng; ++bi) {
     if (stored[bi]) continue;
     const Bucket& b = p.buckets[bi];
     const BucketPtrs q = bucket_ptrs(b, ws);

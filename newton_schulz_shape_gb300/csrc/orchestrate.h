@@ -25,6 +25,8 @@ using nsplan::Tensor;
 int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out);
 // GEMM tiling forced by ns_set_gemm_cluster (0: automatic).
 int gemm_cluster_override();
+// Whether buckets marked small run as one CTA per matrix (ns_set_small_path).
+bool small_path_enabled();
 // Test support: the wait limit armed by ns_test_stall_next_gemm (0 if none),
 // cleared by this call; the launch that takes it stalls.
 unsigned long long take_gemm_stall();
@@ -43,8 +45,8 @@ int make_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_
 int make_epi_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count);
 
 // Launch kinds of ns_profile_read.
-constexpr int kKinds = 6;
-enum { K_GRAM = 0, K_A2B = 1, K_BX = 2, K_PRO = 3, K_PACK = 4, K_BX_FINAL = 5 };
+constexpr int kKinds = 7;
+enum { K_GRAM = 0, K_A2B = 1, K_BX = 2, K_PRO = 3, K_PACK = 4, K_BX_FINAL = 5, K_SMALL = 6 };
 // Count a launch of `kind`; when timing is on, hand out two events for it.
 bool prof_begin(int kind, cudaEvent_t* a, cudaEvent_t* b);
 // Queue the bracketing events of a timed launch for ns_profile_read.
@@ -84,6 +86,14 @@ size_t group_matrices(const Plan& p, size_t b0, size_t b1);
 // the S rank buffers.
 int prologue_bf16(const Plan& p, const void* const* in, void* const* out, char* ws, unsigned int* status,
                   cudaStream_t st, const void* const* rank_in = nullptr);
+// Buckets [0, gemm_buckets(p)) run through the GEMM launches; the rest (small
+// buckets, when the one-CTA-per-matrix path is on) through small_bf16.
+size_t gemm_buckets(const Plan& p);
+// The whole iteration of every small bucket, one CTA per matrix, inputs from
+// `in` (or with rank_in from the S rank buffers, row shards along dim 0) and
+// results to `out` (or with rank_out to the rank buffers).
+int small_bf16(const Plan& p, const void* const* in, void* const* out, unsigned int* status, cudaStream_t st,
+               const void* const* rank_in = nullptr, void* const* rank_out = nullptr);
 // Whether every bucket group's last B*X launch can store its results itself.
 bool final_stores_all(const Plan& p);
 // k steps of (Gram, A*A + B, B*X) and the final store (into `out`, or with

@@ -192,6 +192,9 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
     // was fused and every launch can store its results
     const bool fused_unpack = fused_pack && !wp.buckets.empty() && final_stores_all(wp);
     if (!wp.buckets.empty()) {
+      rc = small_bf16(wp, ins.data(), outs.data(), status, pd.gemm, fused_pack ? rank_in : nullptr,
+                      fused_unpack ? rank_out : nullptr);
+      if (rc != NS_OK) return rc;
       rc = steps_bf16(wp, outs.data(), ws, nsm, status, pd.gemm, fused_unpack ? rank_out : nullptr);
       if (rc != NS_OK) return rc;
     }

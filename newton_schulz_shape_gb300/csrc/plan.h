@@ -43,6 +43,7 @@ struct Bucket {
   uint64_t off_coef = 0;     // fp32 Gram-space: 3 floats per member (Q coefficients)
   int64_t nchunks = 0;       // sum-of-squares chunks per matrix
   bool gram_space = false;   // fp32: run this bucket in Gram space (NS_FP32_GRAM_SPACE, or NS_FP32_AUTO with n >= 2m)
+  bool small = false;        // bf16, m <= 128, n <= 512: may run as one CTA per matrix (small.cu)
 };
 
 struct Plan {

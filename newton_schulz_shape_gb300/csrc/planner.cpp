@@ -107,8 +107,12 @@ int finish(Plan& p, bool keep_homes = false) {
     }
     p.buckets[it->second].members.push_back(i);
   }
+  for (Bucket& b : p.buckets)
+    b.small = p.gram_mode == NS_BF16 && b.m <= nsk::SMALL_MAX_M && b.n <= nsk::SMALL_MAX_N;
   std::stable_sort(p.buckets.begin(), p.buckets.end(), [](const Bucket& x, const Bucket& y) {
-    // per-matrix work ~ m^2 n
+    // buckets that can run one CTA per matrix last (the GEMM launches then
+    // cover a prefix), otherwise heaviest per-matrix work (~ m^2 n) first
+    if (x.small != y.small) return y.small;
     const double wx = double(x.m) * double(x.m) * double(x.n);
     const double wy = double(y.m) * double(y.m) * double(y.n);
     return wx > wy;

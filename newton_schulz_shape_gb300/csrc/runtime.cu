@@ -31,6 +31,7 @@ int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
 // test support: wait limit (ns) of the next bf16 GEMM launch, which then
 // stalls (0: none armed)
 std::atomic<unsigned long long> g_stall_next{0};
+std::atomic<int> g_small_path{1};  // small buckets: one CTA per matrix
 
 // ----------------------------------------------------------- measurement
 std::mutex g_prof_mu;
@@ -73,6 +74,8 @@ void prof_end(int kind, cudaEvent_t a, cudaEvent_t b) {
 }
 
 unsigned long long take_gemm_stall() { return g_stall_next.exchange(0); }
+
+bool small_path_enabled() { return g_small_path.load() != 0; }
 
 int gemm_cluster_override() {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -164,6 +167,12 @@ int ns_set_gemm_cluster(int cl) {
   if (cl != 0 && cl != 1 && cl != 3) return NS_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_cl = cl;
+  return NS_OK;
+}
+
+int ns_set_small_path(int enable) {
+  if (enable != 0 && enable != 1) return NS_ERR_ARG;
+  g_small_path.store(enable);
   return NS_OK;
 }
 
