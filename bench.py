@@ -97,16 +97,27 @@ def view_mn(shape):
     return min(rows, cols), max(rows, cols)
 
 
-def flops_by_kind(shapes, k):
+def is_small(shape) -> bool:
+    """The library runs bf16 matrices with m <= 128 and n <= 512 as one CTA
+    per matrix (kind "small") unless its small path is switched off."""
+    m, n = view_mn(shape)
+    return m <= 128 and n <= 512
+
+
+def flops_by_kind(shapes, k, small_path=True):
     """Algorithmic flops per call by kernel kind: Gram 2 m^2 n, A*A 2 m^3,
-    B*X 2 m^2 n per matrix per step (useful total k (4 m^2 n + 2 m^3))."""
-    g = a2 = bx = 0
+    B*X 2 m^2 n per matrix per step (useful total k (4 m^2 n + 2 m^3));
+    all three of a small matrix's products count for kind "small"."""
+    g = a2 = bx = sm = 0
     for s in shapes:
         m, n = view_mn(s)
+        if small_path and is_small(s):
+            sm += k * (4 * m * m * n + 2 * m * m * m)
+            continue
         g += 2 * m * m * n * k
         a2 += 2 * m * m * m * k
         bx += 2 * m * m * n * k
-    return {"gram": g, "a2b": a2, "bx": bx}
+    return {"gram": g, "a2b": a2, "bx": bx, "small": sm}
 
 
 # NVIDIA's dense (no 2:4 sparsity) bf16 tensor-core figure for one GB300 GPU
@@ -118,13 +129,18 @@ def executed_flops_by_kind(shapes, k, cluster_mode: int = 0):
     the zero-padded operands, only the upper tiles of the symmetric products,
     spare half pairs of odd tile-row counts included. Useful flops
     (flops_by_kind) can exceed the tensor-pipe rate because SYRK skips work."""
-    ex = {"gram": 0, "a2b": 0, "bx": 0}
+    ex = {"gram": 0, "a2b": 0, "bx": 0, "small": 0}
+    big = [s for s in shapes if not is_small(s)]
     for s in shapes:
         m, n = view_mn(s)
         m_pad, n_pad = -(-m // 128) * 128, -(-n // 64) * 64
+        if is_small(s):
+            # the whole padded products: 128 x 128 x n_pad, 128^3, 128 x n_pad x 128
+            ex["small"] += k * (2 * 128 * 128 * n_pad * 2 + 2 * 128 ** 3)
+            continue
         tm, tn_sym, tn_bx = m_pad // 128, -(-m_pad // 256), -(-n_pad // 256)
         for kind, kdim in (("gram", n_pad), ("a2b", m_pad), ("bx", m_pad)):
-            mode = int(gemm_kernel_for(kind, cluster_mode, shapes)[0].startswith("ns_gemm2sm")) if tm >= 2 else 0
+            mode = int(gemm_kernel_for(kind, cluster_mode, big)[0].startswith("ns_gemm2sm")) if tm >= 2 else 0
             if kind == "bx":
                 tiles = (-(-tm // 2) * 2 if mode else tm) * tn_bx
             elif mode:
@@ -148,8 +164,11 @@ def peaks():
 def gemm_kernel_for(kind: str, cluster_mode: int, shapes=()):
     """(kernel name, source file) of the GEMM kind under a tiling mode: the
     library's default runs the 2-SM kernel for Gram, and for A*A and B*X when
-    every bucket has an even number of 128-row tile rows (else the 1-SM one)."""
-    even = all(((view_mn(s)[0] + 127) // 128) % 2 == 0 for s in shapes)
+    every bucket has an even number of 128-row tile rows (else the 1-SM one);
+    small matrices run in ns_small_kernel."""
+    if kind == "small":
+        return "ns_small_kernel", "small.cu"
+    even = all(((view_mn(s)[0] + 127) // 128) % 2 == 0 for s in shapes if not is_small(s))
     mode = cluster_mode if cluster_mode else (3 if kind == "gram" or even else 1)
     if mode == 3:
         return f"ns_gemm2sm_kernel<{kind}>", "gemm2sm.cu"
@@ -662,9 +681,10 @@ def run_ours(args):
         tot = d["bx"]
         d["bx"] = tot * launches.get("bx", 0) / max(1, n_bx)
         d["bx_final"] = tot - d["bx"]
-    gemm_kinds = ["gram", "a2b", "bx", "bx_final"]
-    # the roofline kernel: the pure GEMM launches with the most time
-    dom = max(["gram", "a2b", "bx"], key=lambda k: kms.get(k, 0.0))
+    gemm_kinds = ["gram", "a2b", "bx", "bx_final", "small"]
+    # the roofline kernel: the pure GEMM launches (or the small-matrix
+    # kernel) with the most time
+    dom = max(["gram", "a2b", "bx", "small"], key=lambda k: kms.get(k, 0.0))
     per_launch_ms = kms[dom] / max(1, launches[dom])
     launches_per_step = launches[dom] / args.steps
     flops_per_launch = fl[dom] / launches_per_step
@@ -674,7 +694,7 @@ def run_ours(args):
     # workload (one NS step of one phase); scale it by this launch's share of
     # that work (waves split a phase into several launches)
     traffic = traffic_for(dom, args.gemm_cluster, ns_shapes) if args.workload == "gpt" and not args.layers \
-        and not args.split_qkv else None
+        and not args.split_qkv and dom != "small" else None
     if traffic is not None:
         traffic = int(traffic * flops_per_launch / (sum(fl[k] for k in gemm_kinds if k.startswith(dom))
                                                     / workloads.STEPS))
@@ -685,6 +705,10 @@ def run_ours(args):
                 "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
                 "useful_tflops_step": useful / (ms_step * 1e-3) / 1e12,
                 "flops_per_launch": flops_per_launch, "avg_launch_ms": per_launch_ms}
+    if dom == "small":
+        roofline["note"] = (f"latency-bound: one CTA per matrix, {n_mats} CTAs on "
+                            f"{torch.cuda.get_device_properties(dev).multi_processor_count} SMs; "
+                            "the fraction is of the whole GPU's peak")
     per_kernel = {k: {"launches_per_step": launches[k] / args.steps, "ms_per_step": kms[k] / args.steps}
                   for k in launches}
     for k in gemm_kinds:

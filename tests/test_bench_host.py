@@ -54,10 +54,24 @@ def test_executed_never_below_useful_for_full_tiles():
         fl = bench.flops_by_kind([shape], 5)
         ex = bench.executed_flops_by_kind([shape], 5)
         assert ex["bx"] == fl["bx"]
-    for shape in [(1000, 3000), (200, 72), (130, 130)]:
+    for shape in [(1000, 3000), (130, 130)]:
         fl = bench.flops_by_kind([shape], 5)
         ex = bench.executed_flops_by_kind([shape], 5)
         assert ex["bx"] > fl["bx"]
+
+
+def test_small_matrices_count_as_one_kind():
+    # m <= 128 and n <= 512: the whole iteration is one kernel; it computes the
+    # padded 128-row products, exactly the useful flops at m = 128, n % 64 == 0
+    fl = bench.flops_by_kind([(128, 256)], 5)
+    ex = bench.executed_flops_by_kind([(128, 256)], 5)
+    assert fl["gram"] == fl["a2b"] == fl["bx"] == 0
+    assert fl["small"] == ex["small"] == 5 * (4 * 128 * 128 * 256 + 2 * 128 ** 3)
+    fl = bench.flops_by_kind([(200, 72)], 5)
+    ex = bench.executed_flops_by_kind([(200, 72)], 5)
+    assert ex["small"] > fl["small"] > 0
+    assert bench.flops_by_kind([(128, 256)], 5, small_path=False)["small"] == 0
+    assert bench.gemm_kernel_for("small", 0, [(128, 256)])[0] == "ns_small_kernel"
 
 
 def test_reference_arm_splits_the_workload_once():

@@ -35,14 +35,19 @@ def test_gemm_wait_runs_out_and_the_device_stays_usable(shape):
     plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=1)
     ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
     assert nsg.ns_check_status(plan) == nsg.NS_OK
-    nsg.ns_test_stall_next_gemm(3_000_000)          # 3 ms
-    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
-    assert nsg.ns_check_status(plan) == nsg.NS_ERR_TIMEOUT
-    assert nsg.ns_check_status(plan) == nsg.NS_OK   # read and cleared
-    # the next call on the same device runs normally and is right
-    outs = [torch.full_like(x, float("nan")) for x in ins]
-    nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
-    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    # a 128-row matrix would otherwise run as one CTA with no GEMM launch
+    nsg.ns_set_small_path(False)
+    try:
+        nsg.ns_test_stall_next_gemm(3_000_000)          # 3 ms
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+        assert nsg.ns_check_status(plan) == nsg.NS_ERR_TIMEOUT
+        assert nsg.ns_check_status(plan) == nsg.NS_OK   # read and cleared
+        # the next call on the same device runs normally and is right
+        outs = [torch.full_like(x, float("nan")) for x in ins]
+        nsg.ns_orthogonalize_batched(plan, ins, outs, ws)
+        assert nsg.ns_check_status(plan) == nsg.NS_OK
+    finally:
+        nsg.ns_set_small_path(True)
     assert rel_err(outs[0], oracle_ns(ts[0])) <= BF16_TOL
 
 
