@@ -623,25 +623,35 @@ def run_ours(args):
         ev_cmp = [torch.cuda.Event() for _ in range(NB)]
         ev_out = [torch.cuda.Event() for _ in range(NB)]
 
+        trace = []   # per step: events around the input copies, the compute and the output copies
+
         def e2e_steps(n):
             for k in range(n):
                 b = k % NB
+                tr = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
                 with torch.cuda.stream(s_in):
                     if k >= NB:
                         s_in.wait_event(ev_cmp[b])     # rin[b] was read by step k - NB
+                    tr[0].record(s_in)
                     for r in range(S):
                         rin[b][r].copy_(rank_host[r], non_blocking=True)
+                    tr[1].record(s_in)
                     ev_in[b].record(s_in)
                 stream.wait_event(ev_in[b])
                 if k >= NB:
                     stream.wait_event(ev_out[b])       # rout[b] was copied out by step k - NB
+                tr[2].record(stream)
                 step(rin[b], rout[b])
+                tr[3].record(stream)
                 ev_cmp[b].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_cmp[b])
+                    tr[4].record(s_out)
                     for r in range(S):
                         hout[b][r].copy_(rout[b][r], non_blocking=True)
+                    tr[5].record(s_out)
                     ev_out[b].record(s_out)
+                trace.append(tr)
 
         e2e_steps(NB)                                   # warm-up of the pipeline
         barrier()
@@ -653,6 +663,7 @@ def run_ours(args):
         e0.record(stream)
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
+        trace.clear()
         e2e_steps(args.steps)
         stream.wait_stream(s_out)
         stream.wait_stream(s_in)
@@ -663,7 +674,16 @@ def run_ours(args):
         # the results of the last step really came back
         ok = all(torch.equal(hout[(args.steps - 1) % NB][r], rank_out[r].cpu()) for r in range(S))
         nbytes = 2 * S * L
+        # per-step timings (ms): each group is the step's S copies of one direction
+        groups = {"h2d_ms": [t[0].elapsed_time(t[1]) for t in trace],
+                  "compute_ms": [t[2].elapsed_time(t[3]) for t in trace],
+                  "d2h_ms": [t[4].elapsed_time(t[5]) for t in trace]}
+        timeline = {k: {"median": statistics.median(v), "max": max(v),
+                        "over_2x_median": sum(x > 2 * statistics.median(v) for x in v)} for k, v in groups.items()}
         e2e = {"value": job_value(n_mats, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
+               "timeline": timeline,
+               "copy_gbs_in_region": {"h2d": nbytes / (timeline["h2d_ms"]["median"] * 1e-3) / 1e9,
+                                      "d2h": nbytes / (timeline["d2h_ms"]["median"] * 1e-3) / 1e9},
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "pipelining": f"copies on their own streams overlap the compute of other steps; ring of {NB} "
                              "buffer sets (device in/out, pinned host out)",

@@ -70,6 +70,14 @@ __device__ __forceinline__ unsigned short* out_row(const SmallParams& p, const S
   return reinterpret_cast<unsigned short*>(p.rank_out[r / sh]) + M.rank_off + static_cast<long long>(r % sh) * M.cols;
 }
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Wait for the MMA group committed to `bar`; false (for every thread) if any
 // thread's bounded wait gave up.
 __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -122,30 +130,66 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
   const int m = tr ? M.cols : M.rows, n = tr ? M.rows : M.cols;
   const int npad = (n + 63) / 64 * 64;
 
-  // ---- load X~_0 (transposed where rows > cols) and the sum of squares
+  // ---- load X~_0 (transposed where rows > cols), all loads in flight at once
+  if (!tr) {
+    // rows of the input are rows of X: 16-byte asynchronous copies straight
+    // into the swizzled layout (unaligned rows element by element)
+    for (int r = warp; r < M.rows; r += SM_THREADS / 32) {
+      const unsigned short* src = in_row(p, M, r);
+      const bool al = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+      for (int c0 = lane * 8; c0 < M.cols; c0 += 32 * 8) {
+        if (al && c0 + 8 <= M.cols) {
+          cp_async16(sX + soff(r, c0), src + c0);
+        } else {
+          for (int k = 0; k < 8 && c0 + k < M.cols; ++k)
+            *reinterpret_cast<unsigned short*>(sX + soff(r, c0 + k)) = src[c0 + k];
+        }
+      }
+    }
+    cp_async_wait_all();
+  } else {
+    // rows of the input are columns of X (cols <= 128: lanes 0..15 hold a row's
+    // 8-element units): LROWS rows per warp in flight, then scattered
+    constexpr int LROWS = 8;
+    for (int r0 = warp * LROWS; r0 < M.rows; r0 += SM_THREADS / 32 * LROWS) {
+      const int c0 = lane * 8;
+      uint4 q[LROWS];
+#pragma unroll
+      for (int j = 0; j < LROWS; ++j) {
+        q[j] = make_uint4(0, 0, 0, 0);
+        const int r = r0 + j;
+        if (r < M.rows && c0 < M.cols) {
+          const unsigned short* src = in_row(p, M, r) + c0;
+          if (c0 + 8 <= M.cols && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+            q[j] = __ldg(reinterpret_cast<const uint4*>(src));
+          } else {
+            unsigned short* h = reinterpret_cast<unsigned short*>(&q[j]);
+            for (int k = 0; k < 8 && c0 + k < M.cols; ++k) h[k] = src[k];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < LROWS; ++j) {
+        const int r = r0 + j;
+        if (r >= M.rows || c0 >= M.cols) continue;
+        const unsigned short* h = reinterpret_cast<const unsigned short*>(&q[j]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c0 + k < M.cols) *reinterpret_cast<unsigned short*>(sX + soff(c0 + k, r)) = h[k];
+      }
+    }
+  }
+  __syncthreads();
+  // sum of squares over X~_0 (padding is zero): thread t takes row t
   float ss = 0.0f;
-  for (int r = warp; r < M.rows; r += SM_THREADS / 32) {
-    const unsigned short* src = in_row(p, M, r);
-    for (int c0 = lane * 8; c0 < M.cols; c0 += 32 * 8) {
-      unsigned short v[8];
-      if (c0 + 8 <= M.cols && (reinterpret_cast<uintptr_t>(src + c0) & 15) == 0) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + c0));
-        *reinterpret_cast<uint4*>(v) = q;
-        if (!tr) *reinterpret_cast<uint4*>(sX + soff(r, c0)) = q;
-      } else {
+  for (int c = 0; c < npad; c += 8) {
+    const uint4 q = *reinterpret_cast<const uint4*>(sX + soff(t, c));
+    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = c0 + k < M.cols ? src[c0 + k] : 0;
-        if (!tr)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (c0 + k < M.cols) *reinterpret_cast<unsigned short*>(sX + soff(r, c0 + k)) = v[k];
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float x = bf(v[k]);
-        ss = fmaf(x, x, ss);
-        if (tr && c0 + k < M.cols) *reinterpret_cast<unsigned short*>(sX + soff(c0 + k, r)) = v[k];
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float x0 = __uint_as_float(w4[k] << 16), x1 = __uint_as_float(w4[k] & 0xFFFF0000u);
+      ss = fmaf(x0, x0, ss);
+      ss = fmaf(x1, x1, ss);
     }
   }
 #pragma unroll
