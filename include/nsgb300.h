@@ -244,7 +244,8 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
 /* [ISS] wave dispatch, single-GPU form. A pipeline splits the plan's
  * participating tensors (bf16 plans only, else NS_ERR_UNSUPPORTED) into at
  * most n_waves waves of consecutive tensors with balanced ns_cost (no wave
- * when no tensor participates; n_waves < 1 is NS_ERR_ARG). The plan must
+ * when no tensor participates; one wave when every shape bucket runs as one
+ * CTA per matrix, see ns_set_small_path; n_waves < 1 is NS_ERR_ARG). The plan must
  * outlive the pipeline. ns_pipeline_run then performs pack ->
  * Newton-Schulz -> unpack for the whole plan, with the same results as
  * ns_pack_to_home + ns_orthogonalize_batched + ns_unpack_from_home. Work runs

@@ -12,7 +12,8 @@
 // Markidis et al. 2018 and Ootomo & Yokota 2022), which keeps fp32-level
 // accuracy; the dropped lo*lo term is ~2^-22 relative.
 //
-// All operands are K-major (rows of 32 fp32 = 128 bytes, 128-byte swizzle):
+// All operands are K-major (K blocks of 16 fp32: rows of 64 bytes, 64-byte
+// swizzle; four 48 KB stages):
 // X is kept both as X (m_pad x n_pad, for the Gram) and X^T (n_pad x m_pad,
 // for B*X), and the B*X epilogue writes both copies of the next X.
 // Structure as in gemm.cu: persistent CTAs, a TMA producer thread, one MMA
@@ -27,10 +28,10 @@ namespace {
 
 using namespace nsptx;
 
-constexpr int BM = 128, BN = 256, BK = 32, UK = 8;
-constexpr int STAGES = 2;
-constexpr uint32_t A_BYTES = BM * BK * 4;  // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 4;  // 32 KB
+constexpr int BM = 128, BN = 256, BK = GEMM32_BK, UK = 8;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 4;  // 8 KB
+constexpr uint32_t B_BYTES = BN * BK * 4;  // 16 KB
 constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // hi and lo of both operands
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
@@ -140,9 +141,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm32_kernel(const __grid_cons
         uint8_t* bh = base + 2 * A_BYTES;
         uint8_t* bl = bh + B_BYTES;
         tma_load_3d(bh, &p.tmbh[b], &full[stage], kb * BK, tn * BN, mat);
-        tma_load_3d(bh + 128 * 128, &p.tmbh[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        tma_load_3d(bh + 128 * BK * 4, &p.tmbh[b], &full[stage], kb * BK, tn * BN + 128, mat);
         tma_load_3d(bl, &p.tmbl[b], &full[stage], kb * BK, tn * BN, mat);
-        tma_load_3d(bl + 128 * 128, &p.tmbl[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        tma_load_3d(bl + 128 * BK * 4, &p.tmbl[b], &full[stage], kb * BK, tn * BN + 128, mat);
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -175,11 +176,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm32_kernel(const __grid_cons
         const uint32_t bl = bh + B_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / UK; ++k) {
-          const uint32_t o = k * (UK * 4);  // 32 bytes per K step inside the 128-byte row
+          const uint32_t o = k * (UK * 4);  // 32 bytes per K step inside the 64-byte row
           const uint32_t first = (kb | k) != 0 ? 1u : 0u;
-          mma_tf32(d_tmem, sdesc_sw128(ah + o, 16, 1024), sdesc_sw128(bh + o, 16, 1024), IDESC, first);
-          mma_tf32(d_tmem, sdesc_sw128(ah + o, 16, 1024), sdesc_sw128(bl + o, 16, 1024), IDESC, 1u);
-          mma_tf32(d_tmem, sdesc_sw128(al + o, 16, 1024), sdesc_sw128(bh + o, 16, 1024), IDESC, 1u);
+          mma_tf32(d_tmem, sdesc_sw64(ah + o, 16, 512), sdesc_sw64(bh + o, 16, 512), IDESC, first);
+          mma_tf32(d_tmem, sdesc_sw64(ah + o, 16, 512), sdesc_sw64(bl + o, 16, 512), IDESC, 1u);
+          mma_tf32(d_tmem, sdesc_sw64(al + o, 16, 512), sdesc_sw64(bh + o, 16, 512), IDESC, 1u);
         }
         mma_commit(&empty[stage]);
         if (++stage == STAGES) {

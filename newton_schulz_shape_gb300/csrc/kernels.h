@@ -97,6 +97,10 @@ struct Gemm32Bucket {
 };
 
 constexpr int GEMM32_MAX_OUT = 3200;
+// K block of the fp32 kernels: 16 fp32 (64-byte rows, 64-byte swizzle), so
+// that a stage (hi and lo of a 128-row A tile and a 256-row B tile) is 48 KB
+// and four stages fit in shared memory
+constexpr int GEMM32_BK = 16;
 
 template <int NOUT>
 struct Gemm32ParamsT {

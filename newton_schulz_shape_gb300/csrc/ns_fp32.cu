@@ -38,14 +38,14 @@ Bucket32Ptrs bucket32_ptrs(const Bucket& b, char* ws) {
   return q;
 }
 
-// 3-D fp32 tensor map over [count][outer][inner], box {32, 128, 1}, 128-byte swizzle.
+// 3-D fp32 tensor map over [count][outer][inner], box {GEMM32_BK, 128, 1}, 64-byte swizzle.
 int make_map32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t count) {
   cuuint64_t dims[3] = {inner, outer, count};
   cuuint64_t strides[2] = {inner * 4, inner * outer * 4};
-  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t box[3] = {nsk::GEMM32_BK, 128, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
 }
@@ -80,7 +80,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
       if (phase == nsk::PH32_GRAM) {
         float* xh = q.x[cur];
         float* xl = xh + q.xs;
-        g.k_blocks = static_cast<int>(b.n_pad / 32);
+        g.k_blocks = static_cast<int>(b.n_pad / nsk::GEMM32_BK);
         g.out_h = q.a;
         g.out_l = q.a + q.as;
         rc = make_map32(&gp.tmah[nb], xh, b.n_pad, b.m_pad, cnt);
@@ -88,7 +88,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
         if (rc == NS_OK) rc = make_map32(&gp.tmbh[nb], xh, b.n_pad, b.m_pad, cnt);
         if (rc == NS_OK) rc = make_map32(&gp.tmbl[nb], xl, b.n_pad, b.m_pad, cnt);
       } else {
-        g.k_blocks = static_cast<int>(b.m_pad / 32);
+        g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM32_BK);
         g.out_h = q.b;
         g.out_l = q.b + q.as;
         g.aux_h = q.a;
@@ -108,7 +108,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
       g.tiles_m = static_cast<int>(b.n_pad / nsk::GEMM_BM);
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
       g.tiles_per_mat = g.tiles_m * g.tiles_n;
-      g.k_blocks = static_cast<int>(b.m_pad / 32);
+      g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM32_BK);
       g.ld = static_cast<int>(b.n_pad);
       g.ld_t = static_cast<int>(b.m_pad);
       g.mat_stride = b.m_pad * b.n_pad;
@@ -193,7 +193,7 @@ int run_sym32(const Plan& p, char* ws, size_t b0, size_t b1, Sel sel, float delt
     g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
     g.ld = static_cast<int>(b.m_pad);
     g.mat_stride = b.m_pad * b.m_pad;
-    g.k_blocks = static_cast<int>(b.m_pad / 32);
+    g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM32_BK);
     float* L = sel(bi, 0);
     float* R = sel(bi, 1);
     float* X = sel(bi, 2);

@@ -90,7 +90,12 @@ int ns_pipeline_create(ns_plan_t* plan, int n_waves, ns_pipeline_t** out) {
     *out = pl;
     return NS_OK;
   }
-  const int W = std::min(n_waves, np);
+  // Waves overlap one wave's prologue with the previous wave's GEMMs. When
+  // every bucket runs as one CTA per matrix there is nothing to overlap, and a
+  // split would only add launches: one wave then.
+  bool all_small = small_path_enabled();
+  for (const nsplan::Bucket& b : p.buckets) all_small = all_small && b.small;
+  const int W = all_small ? 1 : std::min(n_waves, np);
   // cost-balanced cut of the participating tensors (index order) into W waves
   double total = 0;
   for (int i : p.part) total += static_cast<double>(std::max<int64_t>(p.t[i].cost, 1));

@@ -301,6 +301,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Same with 64-byte swizzle (layout 4): K-major rows of 64 bytes, 8-row
+// groups SBO = 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 / kind::tf32, fp32 accumulator.
 //   bits 4-5 D type (1 = f32); 7-9 A type; 10-12 B type (bf16 = 1, tf32 = 2);
 //   bit 15 A MN-major; bit 16 B MN-major; 17-22 N >> 3; 24-28 M >> 4.

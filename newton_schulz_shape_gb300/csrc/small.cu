@@ -19,7 +19,9 @@
 // TMEM: Gram accumulator in columns [0, 128), A*A in [128, 256), B*X in
 // [0, n_pad).
 //
-// 128 threads; thread t owns row t (TMEM lane t) in every epilogue. Thread 0
+// 512 threads (16 warps): in every epilogue warp w owns rows [32 (w % 4), +32)
+// (the TMEM lanes that warp may read) and every fourth 32-column chunk starting
+// at chunk w / 4, so four warps share each SM sub-partition's work. Thread 0
 // issues the MMAs (M = 128, K = 16 per instruction) and commits them to an
 // mbarrier that every thread waits on (bounded). The normalisation is folded
 // into the first step as in the GEMM path: X~_0 holds the input unscaled, the
@@ -38,7 +40,8 @@ namespace {
 
 using namespace nsptx;
 
-constexpr int SM_THREADS = 128;
+constexpr int SM_THREADS = 512;
+constexpr int SM_WARPS = SM_THREADS / 32;
 constexpr uint32_t CHUNK = 128 * 128;  // bytes of one 64-column chunk of 128 rows
 
 __host__ __device__ constexpr size_t small_smem_bytes(int n_pad) {
@@ -95,14 +98,16 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
   uint8_t* sB = sA + 2 * CHUNK;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sB + 2 * CHUNK);  // [0] MMA groups, [1] drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
-  float* red = reinterpret_cast<float*>(tmem_slot + 2);  // 4 warp partial sums
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 4);
+  float* red = reinterpret_cast<float*>(tmem_slot + 2);  // SM_WARPS warp partial sums
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + SM_WARPS);
 
   if (blockDim.x != SM_THREADS || blockIdx.x >= static_cast<unsigned>(p.count)) {
     if (threadIdx.x == 0) atomicOr(p.status, NS_DEV_BAD_LAUNCH);
     return;
   }
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  const int lq = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
+  const int row = 32 * lq + lane;           // the row this thread owns in the epilogues
   const uint32_t tmem_cols = NPL > 256 ? 512u : 256u;
   if (t == 0) {
     mbar_init(&bar[0], 1);
@@ -179,34 +184,43 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
       }
     }
   }
-  __syncthreads();
-  // sum of squares over X~_0 (padding is zero): thread t takes row t
-  float ss = 0.0f;
-  for (int c = 0; c < npad; c += 8) {
-    const uint4 q = *reinterpret_cast<const uint4*>(sX + soff(t, c));
-    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float x0 = __uint_as_float(w4[k] << 16), x1 = __uint_as_float(w4[k] & 0xFFFF0000u);
-      ss = fmaf(x0, x0, ss);
-      ss = fmaf(x1, x1, ss);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp] = ss;
   fence_proxy_async_smem();  // X~_0 written by generic stores, read by the tensor cores
   __syncthreads();
-  const double tot = double(red[0]) + double(red[1]) + double(red[2]) + double(red[3]);
-  const float s = static_cast<float>(1.0 / (sqrt(tot) + double(p.eps)));
+  // The scale s = 1 / (||X~_0||_F + eps) comes from the first Gram's diagonal:
+  // ||X~_0||_F^2 = trace(X~_0 X~_0^T), the same exact bf16 products summed in
+  // fp32, so the first product starts right after the load. Zero steps have
+  // no Gram: sum the squares directly.
+  float s = 1.0f;
+  if (p.steps == 0) {
+    float ss = 0.0f;
+    for (int c = 8 * cq; c < npad; c += 32) {
+      const uint4 q = *reinterpret_cast<const uint4*>(sX + soff(row, c));
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x0 = __uint_as_float(w4[k] << 16), x1 = __uint_as_float(w4[k] & 0xFFFF0000u);
+        ss = fmaf(x0, x0, ss);
+        ss = fmaf(x1, x1, ss);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    // fixed-order fp32 sum of the warp partials (FP64 arithmetic is slow on
+    // this part, and every thread needs the scale)
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < SM_WARPS; ++w) tot += red[w];
+    s = 1.0f / (sqrtf(tot) + p.eps);
+  }
 
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(lq * 32) << 16);
   const uint32_t xs = smem_u32(sX), as = smem_u32(sA), bs = smem_u32(sB);
   constexpr uint32_t ID128 = idesc_make(1u, 128, 128, false, false);
   uint32_t ph = 0;
   bool ok = true;
   for (int step = 0; ok && step < p.steps; ++step) {
-    const float sc = step == 0 ? s : 1.0f;
     // ---- A = X X^T (K = n)
     if (t == 0) {
       tc_fence_after();
@@ -220,12 +234,28 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
     ph ^= 1u;
     tc_fence_after();
     {
+      const int c = 32 * cq;
+      uint32_t v[32];
+      tmem_ld32(lane_base + c, v);
+      tmem_ld_wait();
+      if (step == 0) {
+        // the warp whose column chunk is its own row block holds the diagonal
+        // A~[row][row] in register `lane`
+        if (cq == lq) {
+          float d = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == lane) d = __uint_as_float(v[j]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          if (lane == 0) red[lq] = d;
+        }
+        __syncthreads();
+        s = 1.0f / (sqrtf(red[0] + red[1] + red[2] + red[3]) + p.eps);
+      }
+      const float sc = step == 0 ? s : 1.0f;
       const float sc2 = sc * sc;
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + c, v);
-        tmem_ld_wait();
+      {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 q;
@@ -233,7 +263,7 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
           q.y = pack2(sc2 * __uint_as_float(v[8 * u + 2]), sc2 * __uint_as_float(v[8 * u + 3]));
           q.z = pack2(sc2 * __uint_as_float(v[8 * u + 4]), sc2 * __uint_as_float(v[8 * u + 5]));
           q.w = pack2(sc2 * __uint_as_float(v[8 * u + 6]), sc2 * __uint_as_float(v[8 * u + 7]));
-          *reinterpret_cast<uint4*>(sA + soff(t, c + 8 * u)) = q;
+          *reinterpret_cast<uint4*>(sA + soff(row, c + 8 * u)) = q;
         }
       }
     }
@@ -252,14 +282,14 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
     if (!(ok = wait_mma(&bar[0], ph, abort_flag, p.status))) break;
     ph ^= 1u;
     tc_fence_after();
-#pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    {
+      const int c = 32 * cq;
       uint32_t v[32];
       tmem_ld32(lane_base + 128 + c, v);
       tmem_ld_wait();
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint4 qa = *reinterpret_cast<const uint4*>(sA + soff(t, c + 8 * u));
+        const uint4 qa = *reinterpret_cast<const uint4*>(sA + soff(row, c + 8 * u));
         const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
         uint32_t wb[4];
 #pragma unroll
@@ -268,12 +298,13 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
           wb[k] = pack2(p.b * a0 + p.c * __uint_as_float(v[8 * u + 2 * k]),
                         p.b * a1 + p.c * __uint_as_float(v[8 * u + 2 * k + 1]));
         }
-        *reinterpret_cast<uint4*>(sB + soff(t, c + 8 * u)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        *reinterpret_cast<uint4*>(sB + soff(row, c + 8 * u)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    const float sc = step == 0 ? s : 1.0f;
     // ---- B*X (K = 128): B K-major, X MN-major; N in pieces of at most 256
     if (t == 0) {
       tc_fence_after();
@@ -292,13 +323,21 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
     ph ^= 1u;
     tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < npad; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(lane_base + c, v);
+    for (int c0 = 32 * cq; c0 < npad; c0 += 256) {
+      // this warp's chunks c0 and c0 + 128: both TMEM loads in flight at once
+      const bool two = c0 + 128 < npad;
+      uint32_t v2[2][32];
+      tmem_ld32(lane_base + c0, v2[0]);
+      if (two) tmem_ld32(lane_base + c0 + 128, v2[1]);
       tmem_ld_wait();
 #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !two) break;
+      const int c = c0 + 128 * h;
+      const uint32_t* v = v2[h];
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
-        uint4* px = reinterpret_cast<uint4*>(sX + soff(t, c + 8 * u));
+        uint4* px = reinterpret_cast<uint4*>(sX + soff(row, c + 8 * u));
         const uint4 qx = *px;
         const uint32_t wx[4] = {qx.x, qx.y, qx.z, qx.w};
         uint32_t wo[4];
@@ -309,6 +348,7 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
                         sc * (p.a * x1 + __uint_as_float(v[8 * u + 2 * k + 1])));
         }
         *px = make_uint4(wo[0], wo[1], wo[2], wo[3]);
+      }
       }
     }
     fence_proxy_async_smem();
@@ -323,11 +363,13 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
       unsigned short* dst = out_row(p, M, r);
       for (int c0 = lane * 8; c0 < M.cols; c0 += 32 * 8) {
         unsigned short v[8];
+        if (!tr) {
+          // row r of X: the 8 elements are one 16-byte unit of the swizzled row
+          *reinterpret_cast<uint4*>(v) = *reinterpret_cast<const uint4*>(sX + soff(r, c0));
+        } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = min(c0 + k, M.cols - 1);
-          const unsigned short h = *reinterpret_cast<const unsigned short*>(sX + (tr ? soff(c, r) : soff(r, c)));
-          v[k] = h;
+          for (int k = 0; k < 8; ++k)
+            v[k] = *reinterpret_cast<const unsigned short*>(sX + soff(min(c0 + k, M.cols - 1), r));
         }
         if (p.steps == 0) {
 #pragma unroll

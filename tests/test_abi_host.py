@@ -284,6 +284,14 @@ def test_pipeline_wave_split_host():
         assert pipe.workspace_bytes > 0
         # two wave workspaces, each at most the whole plan's
         assert pipe.workspace_bytes <= 2 * plan.workspace_bytes() + 2048
+    # every bucket small (one CTA per matrix): one wave, unless that path is off
+    small = nsg.ns_plan_create([(128, 256)] * 16, S=8)
+    assert nsg.ns_pipeline_create(small, 4).n_waves == 1
+    nsg.ns_set_small_path(False)
+    try:
+        assert nsg.ns_pipeline_create(small, 4).n_waves == 4
+    finally:
+        nsg.ns_set_small_path(True)
     fp32 = nsg.ns_plan_create([(128, 256)], gram_mode=nsg.NS_FP32_GRAM, S=1)
     with pytest.raises(nsg.NsError) as e:
         nsg.ns_pipeline_create(fp32, 2)
