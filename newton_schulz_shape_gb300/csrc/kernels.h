@@ -111,6 +111,7 @@ struct Gemm32ParamsT {
   Gemm32Bucket bk[GEMM_MAX_BUCKETS];
   long long total_tiles;
   int nb;
+  int pair;            // 2-SM form: work items are pairs of 128-row tiles (rows 2q, 2q + 1)
   float alpha, beta, gamma;
   unsigned int* status;
   unsigned long long out_tab[NOUT];
@@ -247,8 +248,10 @@ cudaError_t launch_scale(const ProParams& p, cudaStream_t st);
 cudaError_t launch_prep(const ProParams& p, cudaStream_t st);
 cudaError_t launch_store(const ProParams& p, cudaStream_t st);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t st);
-cudaError_t launch_gemm32(int phase, const Gemm32Params& p, int grid, cudaStream_t st);
-cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int grid, cudaStream_t st);
+// fp32 split-TF32 GEMMs; p.pair selects the 2-SM form (clusters of two CTAs,
+// tcgen05 cta_group::2), which needs every bucket to have >= 2 tile rows.
+cudaError_t launch_gemm32(int phase, const Gemm32Params& p, int nsm, cudaStream_t st);
+cudaError_t launch_gemm32_final(const Gemm32FinalParams& p, int nsm, cudaStream_t st);
 cudaError_t launch_ridge32(const Ridge32Params& p, cudaStream_t st);
 cudaError_t launch_prep32(const ProParams& p, cudaStream_t st);
 cudaError_t launch_store32(const ProParams& p, cudaStream_t st);

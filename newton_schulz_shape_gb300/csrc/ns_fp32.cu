@@ -50,6 +50,20 @@ int make_map32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint6
   return r == CUDA_SUCCESS ? NS_OK : NS_ERR_CUDA;
 }
 
+// The 2-SM form (pairs of 128-row tiles on a cluster of two CTAs) for a
+// launch whose buckets all have at least two tile rows in the phase's M
+// dimension (m_pad for the symmetric products, n_pad for (B X)^T), unless the
+// 1-SM tiling is forced (ns_set_gemm_cluster(1)). Both give identical bits.
+bool pair32(const Plan& p, size_t b0, size_t b1, int phase) {
+  if (gemm_cluster_override() == 1) return false;
+  for (size_t bi = b0; bi < b1; ++bi) {
+    const Bucket& b = p.buckets[bi];
+    const int64_t rows = phase == nsk::PH32_BXT ? b.n_pad : b.m_pad;
+    if (rows / nsk::GEMM_BM < 2) return false;
+  }
+  return true;
+}
+
 template <typename P>
 int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, size_t b1, unsigned int* status,
                  void* const* final_out) {
@@ -58,6 +72,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
   gp.beta = p.b;
   gp.gamma = p.c;
   gp.status = status;
+  gp.pair = pair32(p, b0, b1, phase) ? 1 : 0;
   long long tiles = 0;
   int nb = 0, n_out = 0;
   for (size_t bi = b0; bi < b1; ++bi, ++nb) {
@@ -74,7 +89,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
     if (phase == nsk::PH32_GRAM || phase == nsk::PH32_A2B) {
       g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
-      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
+      g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n, gp.pair ? 2 : 1));
       g.ld = static_cast<int>(b.m_pad);
       g.mat_stride = b.m_pad * b.m_pad;
       if (phase == nsk::PH32_GRAM) {
@@ -107,7 +122,7 @@ int fill_phase32(P& gp, const Plan& p, char* ws, int phase, int cur, size_t b0, 
       float* xn = q.x[1 - cur];
       g.tiles_m = static_cast<int>(b.n_pad / nsk::GEMM_BM);
       g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
-      g.tiles_per_mat = g.tiles_m * g.tiles_n;
+      g.tiles_per_mat = (gp.pair ? (g.tiles_m + 1) / 2 : g.tiles_m) * g.tiles_n;
       g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM32_BK);
       g.ld = static_cast<int>(b.n_pad);
       g.ld_t = static_cast<int>(b.m_pad);
@@ -176,6 +191,7 @@ int run_sym32(const Plan& p, char* ws, size_t b0, size_t b1, Sel sel, float delt
   nsk::Gemm32Params gp;
   std::memset(&gp, 0, sizeof(gp));
   gp.status = status;
+  gp.pair = pair32(p, b0, b1, nsk::PH32_A2B) ? 1 : 0;
   long long tiles = 0;
   int nb = 0;
   for (size_t bi = b0; bi < b1; ++bi, ++nb) {
@@ -190,7 +206,7 @@ int run_sym32(const Plan& p, char* ws, size_t b0, size_t b1, Sel sel, float delt
     g.cols_valid = static_cast<int>(b.m_pad);
     g.tiles_m = static_cast<int>(b.m_pad / nsk::GEMM_BM);
     g.tiles_n = static_cast<int>((b.m_pad + nsk::GEMM_BN - 1) / nsk::GEMM_BN);
-    g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n));
+    g.tiles_per_mat = static_cast<int>(syrk_tiles(g.tiles_m, g.tiles_n, gp.pair ? 2 : 1));
     g.ld = static_cast<int>(b.m_pad);
     g.mat_stride = b.m_pad * b.m_pad;
     g.k_blocks = static_cast<int>(b.m_pad / nsk::GEMM32_BK);
@@ -215,8 +231,7 @@ int run_sym32(const Plan& p, char* ws, size_t b0, size_t b1, Sel sel, float delt
   }
   gp.nb = nb;
   gp.total_tiles = tiles;
-  const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-  return counted(nsk::PH32_A2B, st, [&] { return nsk::launch_gemm32(nsk::PH32_A2B, gp, grid, st); }) ==
+  return counted(nsk::PH32_A2B, st, [&] { return nsk::launch_gemm32(nsk::PH32_A2B, gp, nsm, st); }) ==
                  cudaSuccess
              ? NS_OK
              : NS_ERR_CUDA;
@@ -275,8 +290,7 @@ int orthogonalize_gram_space(const Plan& p, const void* const* in, void* const* 
       nsk::Gemm32Params gp;
       int rc = fill_phase32(gp, p, ws, nsk::PH32_GRAM, 0, b0, b1, status, nullptr);
       if (rc != NS_OK) return rc;
-      const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-      if (counted(nsk::PH32_GRAM, st, [&] { return nsk::launch_gemm32(nsk::PH32_GRAM, gp, grid, st); }) !=
+      if (counted(nsk::PH32_GRAM, st, [&] { return nsk::launch_gemm32(nsk::PH32_GRAM, gp, nsm, st); }) !=
           cudaSuccess)
         return NS_ERR_CUDA;
     }
@@ -371,8 +385,7 @@ int orthogonalize_gram_space(const Plan& p, const void* const* in, void* const* 
         if (rc == NS_OK) rc = make_map32(&gp.tmbl[nb], gs.p[pcur[bi]] + gs.as, b.m_pad, b.m_pad, cnt);
         if (rc != NS_OK) return rc;
       }
-      const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-      if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
+      if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, nsm, st); }) != cudaSuccess)
         return NS_ERR_CUDA;
     } else {
       return NS_ERR_UNSUPPORTED;  // more matrices than one final launch can address
@@ -437,16 +450,14 @@ int orthogonalize_f32(const Plan& p, const void* const* in, void* const* out, ch
           static thread_local nsk::Gemm32FinalParams gp;
           rc = fill_phase32(gp, p, ws, phase, cur, b0, b1, status, out);
           if (rc != NS_OK) return rc;
-          const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-          if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, grid, st); }) != cudaSuccess)
+          if (counted(K_BX_FINAL, st, [&] { return nsk::launch_gemm32_final(gp, nsm, st); }) != cudaSuccess)
             return NS_ERR_CUDA;
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
           nsk::Gemm32Params gp;
           rc = fill_phase32(gp, p, ws, phase, cur, b0, b1, status, nullptr);
           if (rc != NS_OK) return rc;
-          const int grid = static_cast<int>(std::min<long long>(gp.total_tiles, nsm));
-          if (counted(phase, st, [&] { return nsk::launch_gemm32(phase, gp, grid, st); }) != cudaSuccess)
+          if (counted(phase, st, [&] { return nsk::launch_gemm32(phase, gp, nsm, st); }) != cudaSuccess)
             return NS_ERR_CUDA;
         }
         if (phase == nsk::PH32_GRAM && p.ridge > 0.0f) {

@@ -192,3 +192,22 @@ def test_fp32_sweep_points_full_size(m, aspect, mode):
         assert 0.5 < f < 1.2, (i, f)
     err = rel_err(outs[0], oracle(ts[0]))
     assert err <= FP32_TOL, (m, aspect, err)
+
+
+# The fp32 products run on CTA pairs (2-SM MMA) when every bucket of a launch
+# has two or more 128-row tiles; ns_set_gemm_cluster(1) forces one CTA per
+# tile. Same products in the same K order: identical bits. Odd tile-row
+# counts (m_pad = 384, 640; n_pad = 640, 1152) leave a spare half pair.
+@pytest.mark.parametrize("mode", [nsg.NS_FP32_GRAM, nsg.NS_FP32_GRAM_SPACE, nsg.NS_FP32_AUTO])
+def test_fp32_pairs_equal_single_cta(mode):
+    shapes = [(384, 640), (640, 384), (300, 1100), (512, 512), (256, 1152)]
+    ts = workloads.gen_tensors(workloads.Workload("pairs", shapes, 0.02, 86))
+    nsg.ns_set_gemm_cluster(1)
+    try:
+        single = run_mode(shapes, ts, mode)
+    finally:
+        nsg.ns_set_gemm_cluster(0)
+    paired = run_mode(shapes, ts, mode)
+    for s, t, a, b in zip(shapes, ts, single, paired):
+        assert torch.equal(a, b), (mode, s)
+        assert rel_err(b, oracle(t)) <= FP32_TOL, (mode, s)
