@@ -744,7 +744,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
                                f"pack -> NS (5 steps) -> unpack",
                    "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS, "gemm_cluster": args.gemm_cluster,
-                   "split_qkv": bool(args.split_qkv), "waves": args.waves,
+                   "split_qkv": bool(args.split_qkv), "waves": pipe.n_waves if pipe is not None else 0,
                    "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
         "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
         "ns_only": ({"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,
