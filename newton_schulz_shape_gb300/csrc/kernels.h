@@ -219,8 +219,11 @@ struct SmallMat {
   int pad;
 };
 
-struct SmallParams {
-  SmallMat mat[SMALL_MAX_MATS];
+// The per-matrix table comes last and is sized per launch (the launcher
+// copies a table of up to N entries into the smallest block that holds it:
+// a large parameter block costs launch time).
+template <int N>
+struct SmallParamsT {
   int count;
   int n_pad;           // largest n rounded up to 64 over the launch (sizes smem and TMEM)
   int steps;
@@ -231,7 +234,9 @@ struct SmallParams {
   const void* rank_in[ROUTE_MAX_RANKS];
   void* rank_out[ROUTE_MAX_RANKS];
   unsigned int* status;
+  SmallMat mat[N];
 };
+using SmallParams = SmallParamsT<SMALL_MAX_MATS>;
 static_assert(sizeof(SmallParams) <= 32764, "kernel parameter block too large");
 
 // ----------------------------------------------------------------- launchers

@@ -29,6 +29,9 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
+#include <cstddef>
+#include <cstring>
 
 #include "kernels.h"
 #include "launch.cuh"
@@ -61,13 +64,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Address of element (r, 0) of row r of the tensor (original orientation).
-__device__ __forceinline__ const unsigned short* in_row(const SmallParams& p, const SmallMat& M, int r) {
+template <typename P>
+__device__ __forceinline__ const unsigned short* in_row(const P& p, const SmallMat& M, int r) {
   if (!p.in_ranks) return reinterpret_cast<const unsigned short*>(M.in) + static_cast<long long>(r) * M.cols;
   const int sh = M.rows / p.S;
   return reinterpret_cast<const unsigned short*>(p.rank_in[r / sh]) + M.rank_off +
          static_cast<long long>(r % sh) * M.cols;
 }
-__device__ __forceinline__ unsigned short* out_row(const SmallParams& p, const SmallMat& M, int r) {
+template <typename P>
+__device__ __forceinline__ unsigned short* out_row(const P& p, const SmallMat& M, int r) {
   if (!p.out_ranks) return reinterpret_cast<unsigned short*>(M.out) + static_cast<long long>(r) * M.cols;
   const int sh = M.rows / p.S;
   return reinterpret_cast<unsigned short*>(p.rank_out[r / sh]) + M.rank_off + static_cast<long long>(r % sh) * M.cols;
@@ -89,7 +94,8 @@ __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, volatil
   return __syncthreads_and(got ? 1 : 0) != 0;
 }
 
-__global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_constant__ SmallParams p) {
+template <typename P>
+__global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NPL = p.n_pad;  // the launch's largest n_pad: sizes shared memory and TMEM
@@ -402,18 +408,44 @@ __global__ void __launch_bounds__(SM_THREADS, 1) ns_small_kernel(const __grid_co
   }
 }
 
+// The kernel with a table of N matrices; the function attribute (shared
+// memory above 48 KB) is set once per device.
+template <int N>
+cudaError_t launch_small_n(const SmallParams& p, size_t smem, cudaStream_t st) {
+  static std::atomic<unsigned long long> attr_set{0};
+  auto kern = ns_small_kernel<SmallParamsT<N>>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(small_smem_bytes(SMALL_MAX_N)));
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  if constexpr (N == SMALL_MAX_MATS) {
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(p.count)), dim3(SM_THREADS), smem, st, p);
+  } else {
+    SmallParamsT<N> q;
+    std::memcpy(&q, &p, offsetof(SmallParams, mat));
+    std::memcpy(q.mat, p.mat, sizeof(SmallMat) * static_cast<size_t>(p.count));
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(p.count)), dim3(SM_THREADS), smem, st, q);
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_small(const SmallParams& p, cudaStream_t st) {
   if (p.count <= 0) return cudaSuccess;
+  if (p.count > SMALL_MAX_MATS) return cudaErrorInvalidValue;
   if (p.n_pad < 64 || p.n_pad > SMALL_MAX_N || p.n_pad % 64) return cudaErrorInvalidValue;
   const size_t smem = small_smem_bytes(p.n_pad);
-  cudaError_t e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(small_smem_bytes(SMALL_MAX_N)));
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(ns_small_kernel, dim3(static_cast<unsigned>(p.count)), dim3(SM_THREADS), smem, st, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (p.count <= 16) return launch_small_n<16>(p, smem, st);
+  if (p.count <= 64) return launch_small_n<64>(p, smem, st);
+  return launch_small_n<SMALL_MAX_MATS>(p, smem, st);
 }
 
 }  // namespace nsk
