@@ -26,11 +26,10 @@
 //   * a slot is reloaded only after its store has finished reading it
 //     (bulk-group wait), and generic accesses are fenced against the async
 //     proxy before TMA touches the slot again.
-// Symmetric phases visit chunks on or above the diagonal only. A diagonal
-// chunk is completed in its slot (lane i also writes its values of columns
-// j > i into row j, column i), so one store covers it; a chunk strictly above
-// the diagonal also writes its transpose straight to global memory, one
-// contiguous 64-byte row segment per store instruction.
+// Symmetric phases store every chunk of the tiles they compute, which are
+// exactly the upper 256 x 256 pair blocks of A or B (kernels.h); nothing is
+// mirrored: the products that read A or B take the rest from the transposed
+// blocks.
 // The final B*X launch writes each result to the caller's tensor (cropped,
 // transposed back where needed) from registers instead of by TMA.
 // Every wait is bounded; on a timeout or abort the warp stops, lets the loads
@@ -53,7 +52,7 @@ constexpr uint32_t EPI_RING_BYTES = EPI_WARPS * EPI_SLOTS * EPI_SLOT_BYTES;  // 
 
 struct EpiTile {
   int b, mat, tm, tn;
-  int ci_lo, ci_hi;  // this warp's chunks [ci_lo, ci_hi) of the tile
+  int ci_hi;  // this warp's chunks [0, ci_hi) of the tile
 };
 
 // Tile t -> its chunks for the warp owning rows [tm*128 + 32*lg, +32).
@@ -65,10 +64,6 @@ __device__ __forceinline__ EpiTile epi_tile(const P& p, const Dec& dec, long lon
   const int c_base = e.tn * GEMM_BN;
   // a pair's second row past the last tile row (odd tiles_m) stores nothing
   e.ci_hi = e.tm < B.tiles_m ? min(GEMM_BN / 32, (B.cols_valid - c_base) / 32) : 0;
-  // symmetric phases: chunks wholly below the diagonal are the mirror of others
-  const int r0w = e.tm * GEMM_BM + lg * 32;
-  e.ci_lo = PHASE != PH_BX ? max(0, (r0w - c_base) / 32) : 0;
-  if (e.ci_lo > e.ci_hi) e.ci_lo = e.ci_hi;
   return e;
 }
 
@@ -86,7 +81,7 @@ __device__ __forceinline__ bool epi_next(const P& p, const Dec& dec, EpiCursor& 
     c.t += tstride;
     if (c.t >= p.total_tiles) return false;
     c.e = epi_tile<PHASE>(p, dec, c.t, lg);
-    c.ci = c.e.ci_lo;
+    c.ci = 0;
   }
   return true;
 }
@@ -108,7 +103,6 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
                                               int lg, int lane, long long t0, long long tstride, uint64_t lim,
                                               uint64_t* tfull,
                                               uint8_t* ring, uint64_t* rfull, volatile int* abort_flag) {
-  constexpr bool SYRK = PHASE != PH_BX;
   constexpr bool AUX = PHASE != PH_GRAM;
   // loads run EPI_SLOTS - 1 jobs ahead of the job being processed
   EpiCursor ld;
@@ -140,7 +134,7 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
       break;
     }
     tc_fence_after();
-    if (e.ci_lo == e.ci_hi) {
+    if (e.ci_hi == 0) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) release(acc);
@@ -149,7 +143,7 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
     const int r = r0w + lane;
     // first step: X~_0 is unscaled, s = 1 / (||T||_F + eps) per matrix
     const float sc = (PHASE != PH_A2B && B.scale) ? B.scale[e.mat] : 1.0f;
-    for (int ci = e.ci_lo; ci < e.ci_hi; ++ci, ++g) {
+    for (int ci = 0; ci < e.ci_hi; ++ci, ++g) {
       const int s = static_cast<int>(g % EPI_SLOTS);
       uint8_t* slot = ring + s * EPI_SLOT_BYTES;
       const int cg = e.tn * GEMM_BN + ci * 32;
@@ -281,28 +275,11 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(slot + epi_swz(lane, u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        if (SYRK && cg == r0w) {
-          // diagonal chunk: the part below the diagonal is the mirror of the
-          // part above it
-          __syncwarp();
-          uint8_t* col = slot + ((lane & 7) << 1);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j > lane)
-              *reinterpret_cast<__nv_bfloat16*>(col + epi_swz(j, lane >> 3)) = hv[j];
-        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_3d(&p.tmo[e.b], slot, cg, r0w, e.mat);
           bulk_commit_group();
-        }
-        if (SYRK && cg != r0w) {
-          // strictly above the diagonal: (r, c) also goes to (c, r)
-          __nv_bfloat16* out =
-              reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(e.mat) * B.out_stride;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) out[static_cast<long long>(cg + j) * B.ld_out + r] = hv[j];
         }
       }
       if (AUX && lane == 0 && more) {

@@ -1,9 +1,14 @@
 // The three tensor-core products of one quintic Newton-Schulz step
 // (Megatron-Core API page owner_planning, ns_cost_fn):
 //
-//   PH_GRAM  A = X X^T                  symmetric: upper tiles only + mirror
-//   PH_A2B   B = b A + c (A A)          symmetric: upper tiles only + mirror
+//   PH_GRAM  A = X X^T                  symmetric: upper pair blocks only
+//   PH_A2B   B = b A + c (A A)          symmetric: upper pair blocks only
 //   PH_BX    X' = a X + B X             full tiles, written to the other X buffer
+//
+// A and B are stored as their upper 256 x 256 pair blocks (kernels.h). A·A
+// and B·X read their symmetric operands K-block by K-block: left of the
+// operand rows' diagonal pair block from the transposed, stored block
+// (MN-major loads, transposed MMA operand), elsewhere as rows (K-major).
 //
 // One persistent kernel per phase, one CTA per SM, a 128 x 256 output tile per
 // work item, tiles of every shape bucket of the launch in one static schedule,
@@ -79,8 +84,9 @@ __device__ __forceinline__ void decode_tile(const P& p, long long t, int& b, int
 template <int PHASE, bool FINAL, typename P>
 __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_constant__ P p) {
   static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
-  constexpr bool B_MN = (PHASE == PH_BX);
-  constexpr uint32_t IDESC = idesc_make(1u, BM, BN, false, B_MN);
+  // symmetric operands stored as upper pair blocks: A of A*A and B*X, B of A*A
+  constexpr bool A_TRI = (PHASE != PH_GRAM);
+  constexpr bool B_TRI = (PHASE == PH_A2B);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -121,7 +127,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
     for (int b = 0; b < p.nb; ++b) {
       prefetch_tmap(&p.tma[b]);
       prefetch_tmap(&p.tmb[b]);
-      if (PHASE != PH_GRAM) prefetch_tmap(&p.tme[b]);
+      if (PHASE != PH_GRAM) {
+        prefetch_tmap(&p.tme[b]);
+        prefetch_tmap(&p.tmt[b]);
+      }
       if (!FINAL) prefetch_tmap(&p.tmo[b]);
     }
   }
@@ -146,15 +155,26 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       int b, mat, tm, tn;
       decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
+      // K-blocks left of the operand rows' diagonal pair block come transposed
+      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
         uint8_t* a_dst = sA + stage * A_BYTES;
         uint8_t* b_dst = sB + stage * B_BYTES;
-        tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
-        if (!B_MN) {
-          tma_load_3d(b_dst, &p.tmb[b], &full[stage], kb * BK, tn * BN, mat);
-          tma_load_3d(b_dst + 128 * 128, &p.tmb[b], &full[stage], kb * BK, tn * BN + 128, mat);
+        if (kb < kb_ta) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_3d(a_dst + j * (64 * 128), &p.tmt[b], &full[stage], tm * BM + j * 64, kb * BK, mat);
+        } else {
+          tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
+        }
+        if (PHASE != PH_BX && kb >= kb_tb) {
+          // K-major rows: X (Gram), or A through the A operand's map (A*A)
+          const CUtensorMap* mb = PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b];
+          tma_load_3d(b_dst, mb, &full[stage], kb * BK, tn * BN, mat);
+          tma_load_3d(b_dst + 128 * 128, mb, &full[stage], kb * BK, tn * BN + 128, mat);
         } else {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
@@ -184,17 +204,23 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, lim)) goto mma_done;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
+      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+        const bool a_mn = kb < kb_ta;
+        const bool b_mn = PHASE == PH_BX || kb < kb_tb;
+        const uint32_t idesc = idesc_make(1u, BM, BN, a_mn, b_mn);
 #pragma unroll
         for (int k = 0; k < BK / UK; ++k) {
-          const uint64_t ad = sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
-          const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+          const uint64_t ad = a_mn ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
+                                   : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+          const uint64_t bd = b_mn ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
-          mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         mma_commit(&empty[stage]);
         if (++stage == STAGES) {

@@ -10,6 +10,11 @@
 // against 48 KB when one SM holds a whole 128 x 256 tile's operands. The
 // accumulator is split by rows: each CTA's TMEM holds its 128 rows x 256
 // fp32 columns, so each CTA's epilogue works exactly as in the 1-SM kernel.
+// A and B are stored as upper pair blocks (kernels.h): the K-blocks of a
+// symmetric operand left of its rows' diagonal pair block are loaded MN-major
+// from the transposed block, and the MMA takes that operand transposed. Both
+// CTAs' A rows lie in pair row q and their B rows in pair row tn, so the
+// choice is the same in both halves of every MMA.
 //
 // Synchronisation (all waits bounded):
 //   full[s]   leader only; count 1 (the leader's arrive.expect_tx of both
@@ -79,8 +84,9 @@ __device__ __forceinline__ void decode_pair(const P& p, long long t, uint32_t ra
 template <int PHASE, bool FINAL, typename P>
 __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_constant__ P p) {
   static_assert(!FINAL || PHASE == PH_BX, "only the B*X phase has a final-store form");
-  constexpr bool B_MN = (PHASE == PH_BX);
-  constexpr uint32_t IDESC = idesc_make(1u, 2 * BM, BN, false, B_MN);
+  // symmetric operands stored as upper pair blocks: A of A*A and B*X, B of A*A
+  constexpr bool A_TRI = (PHASE != PH_GRAM);
+  constexpr bool B_TRI = (PHASE == PH_A2B);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -123,7 +129,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
     for (int b = 0; b < p.nb; ++b) {
       prefetch_tmap(&p.tma[b]);
       prefetch_tmap(&p.tmb[b]);
-      if (PHASE != PH_GRAM) prefetch_tmap(&p.tme[b]);
+      if (PHASE != PH_GRAM) {
+        prefetch_tmap(&p.tme[b]);
+        prefetch_tmap(&p.tmt[b]);
+      }
       if (!FINAL) prefetch_tmap(&p.tmo[b]);
     }
   }
@@ -152,19 +161,30 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       int b, mat, tm, tn;
       decode_pair<PHASE>(p, t, rank, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
+      // K-blocks left of the operand rows' diagonal pair block come transposed
+      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         const uint32_t full_l = map_to_rank(&full[stage], 0);
         if (leader) mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
-        tma_load_3d_pair(sA + stage * A_BYTES, &p.tma[b], full_l, kb * BK, tm * BM, mat);
+        uint8_t* a_dst = sA + stage * A_BYTES;
+        if (kb < kb_ta) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            tma_load_3d_pair(a_dst + j * (64 * 128), &p.tmt[b], full_l, tm * BM + j * 64, kb * BK, mat);
+        } else {
+          tma_load_3d_pair(a_dst, &p.tma[b], full_l, kb * BK, tm * BM, mat);
+        }
         uint8_t* b_dst = sB + stage * B_BYTES;
         const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
-        if (!B_MN) {
-          tma_load_3d_pair(b_dst, &p.tmb[b], full_l, kb * BK, n0, mat);
-        } else {
+        if (PHASE == PH_BX || kb < kb_tb) {
 #pragma unroll
           for (int j = 0; j < BN / 128; ++j)
             tma_load_3d_pair(b_dst + j * (64 * 128), &p.tmb[b], full_l, n0 + j * 64, kb * BK, mat);
+        } else {
+          // K-major rows: X (Gram), or A through the A operand's map (A*A)
+          tma_load_3d_pair(b_dst, PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b], full_l, kb * BK, n0, mat);
         }
         ++issued;
         if (++stage == STAGES) {
@@ -189,17 +209,23 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, lim)) goto mma_done;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
+      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+        const bool a_mn = kb < kb_ta;
+        const bool b_mn = PHASE == PH_BX || kb < kb_tb;
+        const uint32_t idesc = idesc_make(1u, 2 * BM, BN, a_mn, b_mn);
 #pragma unroll
         for (int k = 0; k < BK / UK; ++k) {
-          const uint64_t ad = sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
-          const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+          const uint64_t ad = a_mn ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
+                                   : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+          const uint64_t bd = b_mn ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
-          mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         mma_commit_pair_mc(&empty[stage], 3);  // both CTAs' copies of the stage are free
         if (++stage == STAGES) {

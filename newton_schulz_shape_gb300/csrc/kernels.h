@@ -40,12 +40,18 @@ struct GemmBucket {
 // out_ranks the results go straight to the S rank buffers instead (row
 // shards along dim 0): the entry is the tensor's shard offset in every rank
 // buffer (elements) shifted left by one, with the same bit 0.
-constexpr int GEMM_MAX_OUT = 3440;
+constexpr int GEMM_MAX_OUT = 3312;
 
+// A and B are stored as their upper 256 x 256 pair blocks only: block rows
+// 256 Q .. 256 Q + 255, columns from 256 Q on, each block in full (the SYRK
+// tiles compute exactly these). A product reading a symmetric operand takes
+// the 64-wide K-blocks left of its rows' diagonal pair block (columns below
+// 256 Q) from the transposed, stored block: the same values, loaded MN-major.
 template <int NOUT>
 struct GemmParamsT {
   CUtensorMap tma[GEMM_MAX_BUCKETS];  // A operand, K-major, box {64, 128, 1}
-  CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} / MN-major box {64,64,1}
+  CUtensorMap tmb[GEMM_MAX_BUCKETS];  // B operand: K-major box {64,128,1} (Gram) / MN-major box {64,64,1}
+  CUtensorMap tmt[GEMM_MAX_BUCKETS];  // A operand MN-major, box {64, 64, 1} (A*A: A; B*X: B)
   // epilogue chunks, box {32, 32, 1}, 64-byte swizzle: aux (A2B: A, BX: X)
   // and output (final-store launches write from registers: no output map)
   CUtensorMap tme[GEMM_MAX_BUCKETS];

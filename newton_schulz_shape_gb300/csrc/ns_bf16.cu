@@ -122,8 +122,11 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
         g.aux = q.a;
         g.ld_aux = static_cast<int>(b.m_pad);
         g.aux_stride = b.m_pad * b.m_pad;
+        // both operands are A (upper pair blocks): rows through tma, the
+        // transposed blocks left of the diagonal through tmt (A) and tmb (B)
         rc = make_map(&gp.tma[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
-        if (rc == NS_OK) rc = make_map(&gp.tmb[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 128);
+        if (rc == NS_OK) rc = make_map(&gp.tmt[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 64);
+        if (rc == NS_OK) rc = make_map(&gp.tmb[nb], q.a, b.m_pad, b.m_pad, cnt, 64, 64);
         if (rc == NS_OK) rc = make_epi_map(&gp.tme[nb], q.a, b.m_pad, b.m_pad, cnt);
         if (rc == NS_OK) rc = tmo ? make_epi_map(tmo, q.b, b.m_pad, b.m_pad, cnt) : NS_ERR_UNSUPPORTED;
       }
@@ -139,6 +142,7 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
       g.out_stride = b.m_pad * b.n_pad;
       g.aux_stride = b.m_pad * b.n_pad;
       rc = make_map(&gp.tma[nb], q.b, b.m_pad, b.m_pad, cnt, 64, 128);
+      if (rc == NS_OK) rc = make_map(&gp.tmt[nb], q.b, b.m_pad, b.m_pad, cnt, 64, 64);
       if (rc == NS_OK) rc = make_map(&gp.tmb[nb], cur, b.n_pad, b.m_pad, cnt, 64, 64);
       if (rc == NS_OK) rc = make_epi_map(&gp.tme[nb], cur, b.n_pad, b.m_pad, cnt);
       if (rc == NS_OK && !final_out) rc = tmo ? make_epi_map(tmo, nxt, b.n_pad, b.m_pad, cnt) : NS_ERR_UNSUPPORTED;
