@@ -54,6 +54,9 @@ def parse():
                     help="keep only the first N layers of the workload (small cases for ncu captures)")
     ap.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 3],
                     help="GEMM tiling: 0 automatic, 1 single CTA, 3 2-SM MMA")
+    ap.add_argument("--sym-store", choices=["upper", "mirror"], default="upper",
+                    help="bf16 A and B: upper 256x256 pair blocks only (readers load the rest "
+                         "transposed) or also their mirror")
     ap.add_argument("--waves", type=int, default=2,
                     help="run the step through the wave pipeline with this many waves (0: serial calls)")
     ap.add_argument("--split-qkv", action="store_true",
@@ -470,6 +473,7 @@ def run_ours(args):
     w = get_workload(args.workload, args.layers)
     w.seed = replica_seed(w.seed, rank, world)
     nsg.ns_set_gemm_cluster(args.gemm_cluster)
+    nsg.ns_set_symmetric_store(1 if args.sym_store == "mirror" else 0)
     S, shapes = w.S, w.shapes
     plan = nsg.ns_plan_create(shapes, steps=workloads.STEPS, eps=workloads.EPS, S=S, shard_dim=0)
     home_off, home_sizes, rank_sizes = plan.home_layout()
@@ -714,7 +718,7 @@ def run_ours(args):
     # workload (one NS step of one phase); scale it by this launch's share of
     # that work (waves split a phase into several launches)
     traffic = traffic_for(dom, args.gemm_cluster, ns_shapes) if args.workload == "gpt" and not args.layers \
-        and not args.split_qkv and dom != "small" else None
+        and not args.split_qkv and dom != "small" and args.sym_store == "upper" else None
     if traffic is not None:
         traffic = int(traffic * flops_per_launch / (sum(fl[k] for k in gemm_kinds if k.startswith(dom))
                                                     / workloads.STEPS))
@@ -744,7 +748,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name}: {n_mats} matrices, S={S} row shards, LPT homes, "
                                f"pack -> NS (5 steps) -> unpack",
                    "matrices": n_mats, "S": S, "ns_steps": workloads.STEPS, "gemm_cluster": args.gemm_cluster,
-                   "split_qkv": bool(args.split_qkv), "waves": pipe.n_waves if pipe is not None else 0,
+                   "symmetric_store": args.sym_store, "split_qkv": bool(args.split_qkv), "waves": pipe.n_waves if pipe is not None else 0,
                    "l2": f"inputs larger than L2 ({2 * S * L / 1e9:.2f} GB of bf16 per step)"},
         "tflops_useful": useful / (ms_step * 1e-3) / 1e12 * world,
         "ns_only": ({"ms": ns_ms, "tflops_useful": useful / (ns_ms * 1e-3) / 1e12,

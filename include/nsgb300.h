@@ -354,6 +354,19 @@ int ns_set_gemm_cluster(int cl);
  * NS_ERR_ARG. Process-wide. */
 int ns_set_small_path(int enable);
 
+/* Tuning: how the bf16 path stores the symmetric matrices A = X X^T and
+ * B = b A + c A^2 (SYRK: only the tiles that touch the upper triangle are
+ * computed; Megatron-Core API page, the symmetric-Gram item of the issue).
+ * Both tilings compute exactly the upper 256 x 256 pair blocks of each
+ * m_pad x m_pad result, in full. mode = 0 (the default): only those blocks
+ * are stored, and the products that read A or B (A*A, B*X) load the K-blocks
+ * left of their rows' diagonal pair block from the stored transposed block
+ * (MN-major). mode = 1: the symmetric products also write the transpose of
+ * every block above the diagonal pair blocks (the mirror), and the readers
+ * take rows only. Other values are NS_ERR_ARG. Process-wide; both modes give
+ * bitwise-identical results (the same products in the same K order). */
+int ns_set_symmetric_store(int mode);
+
 /* enable != 0 turns per-launch event timing on, 0 off. Process-wide. */
 int ns_profile_enable(int enable);
 

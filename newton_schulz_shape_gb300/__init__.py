@@ -271,6 +271,12 @@ def ns_set_small_path(enable: bool) -> None:
     check(lib.ns_set_small_path(1 if enable else 0), "ns_set_small_path")
 
 
+def ns_set_symmetric_store(mode: int) -> None:
+    """bf16 A and B: 0 stores only the upper 256 x 256 pair blocks (readers
+    take the rest transposed; the default), 1 also stores the mirror."""
+    check(lib.ns_set_symmetric_store(mode), "ns_set_symmetric_store")
+
+
 class NsPipeline:
     """Owns an ns_pipeline_t* (wave-dispatched pack -> NS -> unpack)."""
 

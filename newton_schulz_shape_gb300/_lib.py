@@ -79,6 +79,7 @@ _SIGS = {
     "ns_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "ns_set_gemm_cluster": (ctypes.c_int, [ctypes.c_int]),
     "ns_set_small_path": (ctypes.c_int, [ctypes.c_int]),
+    "ns_set_symmetric_store": (ctypes.c_int, [ctypes.c_int]),
     "ns_profile_read": (ctypes.c_int, [ctypes.c_int, _i64p, ctypes.POINTER(ctypes.c_double)]),
 }
 

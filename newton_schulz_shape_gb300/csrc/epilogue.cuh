@@ -27,9 +27,12 @@
 //     (bulk-group wait), and generic accesses are fenced against the async
 //     proxy before TMA touches the slot again.
 // Symmetric phases store every chunk of the tiles they compute, which are
-// exactly the upper 256 x 256 pair blocks of A or B (kernels.h); nothing is
-// mirrored: the products that read A or B take the rest from the transposed
-// blocks.
+// exactly the upper 256 x 256 pair blocks of A or B (kernels.h). By default
+// nothing is mirrored: the products that read A or B take the rest from the
+// transposed blocks. With p.mirror, a tile right of its rows' diagonal pair
+// block also writes its transpose straight to global memory (lanes hold
+// consecutive rows: one contiguous 64-byte segment per store instruction);
+// the diagonal pair blocks are computed in full and need no mirror.
 // The final B*X launch writes each result to the caller's tensor (cropped,
 // transposed back where needed) from registers instead of by TMA.
 // Every wait is bounded; on a timeout or abort the warp stops, lets the loads
@@ -103,6 +106,7 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
                                               int lg, int lane, long long t0, long long tstride, uint64_t lim,
                                               uint64_t* tfull,
                                               uint8_t* ring, uint64_t* rfull, volatile int* abort_flag) {
+  constexpr bool SYRK = PHASE != PH_BX;
   constexpr bool AUX = PHASE != PH_GRAM;
   // loads run EPI_SLOTS - 1 jobs ahead of the job being processed
   EpiCursor ld;
@@ -280,6 +284,13 @@ __device__ __forceinline__ void epilogue_warp(const P& p, const Dec& dec, const 
         if (lane == 0) {
           tma_store_3d(&p.tmo[e.b], slot, cg, r0w, e.mat);
           bulk_commit_group();
+        }
+        if (SYRK && p.mirror && e.tn > e.tm / 2) {
+          // right of the diagonal pair block: (r, c) also goes to (c, r)
+          __nv_bfloat16* o =
+              reinterpret_cast<__nv_bfloat16*>(B.out) + static_cast<long long>(e.mat) * B.out_stride;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[static_cast<long long>(cg + j) * B.ld_out + r] = hv[j];
         }
       }
       if (AUX && lane == 0 && more) {

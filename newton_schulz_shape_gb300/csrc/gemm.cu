@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       decode_tile<PHASE>(p, t, b, mat, tm, tn);
       const int kb_n = p.bk[b].k_blocks;
       // K-blocks left of the operand rows' diagonal pair block come transposed
-      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
-      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
+      const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, lim)) goto mma_done;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      const int kb_ta = A_TRI ? (tm / 2) * (2 * BM / BK) : 0;
-      const int kb_tb = B_TRI ? tn * (BN / BK) : 0;
+      const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
+      const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();

@@ -61,6 +61,7 @@ struct GemmParamsT {
   int nb;
   float alpha, beta, gamma;  // a, b, c of the quintic step
   int reverse;               // walk the tiles last to first (serpentine order across launches)
+  int mirror;                // symmetric outputs also store their mirror; readers of A and B take rows only
   // Test support: wait_ns (0 = NS_WAIT_LIMIT_NS) bounds every mbarrier wait of
   // the launch; stall != 0 makes the TMA producer issue no copy at all, so the
   // MMA issuer's first wait for operands runs out after wait_ns and the

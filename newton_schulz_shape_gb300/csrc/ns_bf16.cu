@@ -172,12 +172,13 @@ int fill_phase(P& gp, const Plan& p, char* ws, int phase, bool cur_is_x0, size_t
 }
 
 int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, size_t b1, int nsm,
-              unsigned int* status, bool first_step, bool reverse, cudaStream_t st) {
+              unsigned int* status, bool first_step, bool reverse, bool mirror, cudaStream_t st) {
   nsk::GemmParams gp;
   const int cl = pick_cl(p, b0, b1, phase);
   int rc = fill_phase(gp, p, ws, phase, cur_is_x0, b0, b1, status, nullptr, count_mode(cl), first_step);
   if (rc != NS_OK) return rc;
   gp.reverse = reverse ? 1 : 0;
+  gp.mirror = mirror ? 1 : 0;
   if (const unsigned long long ns = take_gemm_stall()) {
     gp.stall = 1;
     gp.wait_ns = ns;
@@ -192,11 +193,13 @@ int run_phase(const Plan& p, char* ws, int phase, bool cur_is_x0, size_t b0, siz
 // B*X phase of the last step, storing results directly into `out`, or with
 // rank_out (row shards along dim 0) into the S rank buffers.
 int run_final_bx(const Plan& p, char* ws, bool cur_is_x0, size_t b0, size_t b1, int nsm, unsigned int* status,
-                 void* const* out, bool first_step, bool reverse, cudaStream_t st, void* const* rank_out = nullptr) {
+                 void* const* out, bool first_step, bool reverse, bool mirror, cudaStream_t st,
+                 void* const* rank_out = nullptr) {
   static thread_local nsk::GemmFinalParams gp;  // ~32 KB: kept off the stack
   const int cl = pick_cl(p, b0, b1, nsk::PH_BX);
   int rc = fill_phase(gp, p, ws, nsk::PH_BX, cur_is_x0, b0, b1, status, out, count_mode(cl), first_step, rank_out);
   gp.reverse = reverse ? 1 : 0;
+  gp.mirror = mirror ? 1 : 0;
   if (rc != NS_OK) return rc;
   if (const unsigned long long ns = take_gemm_stall()) {
     gp.stall = 1;
@@ -355,6 +358,8 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
   // table fits the parameter block; other groups go through the store kernel.
   const size_t ng = gemm_buckets(p);
   std::vector<char> stored(ng, 0);
+  // one storage mode for every product of the call
+  const bool mirror = symmetric_mirror();
   bool cur_is_x0 = true;
   for (int step = 0; step < p.steps; ++step) {
     const bool last = step + 1 == p.steps;
@@ -365,10 +370,10 @@ int steps_bf16(const Plan& p, void* const* out, char* ws, int nsm, unsigned int*
         // starting on the matrices the previous product wrote last (still in L2)
         const bool serp = ((step * 3 + phase) & 1) != 0;
         if (last && phase == nsk::PH_BX && group_matrices(p, b0, b1) <= size_t(nsk::GEMM_MAX_OUT)) {
-          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, serp, st, rank_out);
+          rc = run_final_bx(p, ws, cur_is_x0, b0, b1, nsm, status, out, step == 0, serp, mirror, st, rank_out);
           for (size_t bi = b0; bi < b1; ++bi) stored[bi] = 1;
         } else {
-          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, serp, st);
+          rc = run_phase(p, ws, phase, cur_is_x0, b0, b1, nsm, status, step == 0, serp, mirror, st);
         }
         if (rc != NS_OK) return rc;
       }

@@ -27,6 +27,8 @@ int device_setup(int* dev_out, unsigned int** status_out, int* nsm_out);
 int gemm_cluster_override();
 // Whether buckets marked small run as one CTA per matrix (ns_set_small_path).
 bool small_path_enabled();
+// Whether the bf16 symmetric products store their mirror (ns_set_symmetric_store).
+bool symmetric_mirror();
 // Test support: the wait limit armed by ns_test_stall_next_gemm (0 if none),
 // cleared by this call; the launch that takes it stalls.
 unsigned long long take_gemm_stall();

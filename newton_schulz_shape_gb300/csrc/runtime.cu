@@ -32,6 +32,7 @@ int g_force_cl = 0;  // 0: automatic; otherwise the tiling mode of pick_cl
 // stalls (0: none armed)
 std::atomic<unsigned long long> g_stall_next{0};
 std::atomic<int> g_small_path{1};  // small buckets: one CTA per matrix
+std::atomic<int> g_sym_mirror{0};  // bf16 A and B: 0 upper pair blocks only, 1 also the mirror
 
 // ----------------------------------------------------------- measurement
 std::mutex g_prof_mu;
@@ -76,6 +77,8 @@ void prof_end(int kind, cudaEvent_t a, cudaEvent_t b) {
 unsigned long long take_gemm_stall() { return g_stall_next.exchange(0); }
 
 bool small_path_enabled() { return g_small_path.load() != 0; }
+
+bool symmetric_mirror() { return g_sym_mirror.load() != 0; }
 
 int gemm_cluster_override() {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -173,6 +176,12 @@ int ns_set_gemm_cluster(int cl) {
 int ns_set_small_path(int enable) {
   if (enable != 0 && enable != 1) return NS_ERR_ARG;
   g_small_path.store(enable);
+  return NS_OK;
+}
+
+int ns_set_symmetric_store(int mode) {
+  if (mode != 0 && mode != 1) return NS_ERR_ARG;
+  g_sym_mirror.store(mode);
   return NS_OK;
 }
 

@@ -298,6 +298,16 @@ def test_pipeline_wave_split_host():
     assert e.value.code == nsg.NS_ERR_UNSUPPORTED
 
 
+def test_symmetric_store_modes():
+    # 0 (upper pair blocks, the default) and 1 (also the mirror); anything else is refused
+    for bad in (-1, 2, 3):
+        with pytest.raises(nsg.NsError) as e:
+            nsg.ns_set_symmetric_store(bad)
+        assert e.value.code == nsg.NS_ERR_ARG
+    nsg.ns_set_symmetric_store(1)
+    nsg.ns_set_symmetric_store(0)
+
+
 def test_pipeline_with_nothing_participating():
     # a plan without participating tensors gives a pipeline of no waves
     for plan in (nsg.ns_plan_create([], S=2),

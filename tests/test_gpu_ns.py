@@ -112,6 +112,29 @@ def test_cluster_pairs_odd_tile_rows(cl):
         assert rel_err(o, oracle_ns(t)) <= BF16_TOL, (cl, s_)
 
 
+@pytest.mark.parametrize("cl", [0, 1, 3])
+def test_symmetric_store_modes_agree(cl):
+    # A and B stored as upper pair blocks (readers take the rest transposed)
+    # or with their mirror (readers take rows): the same products in the same
+    # K order, so bitwise-equal results; odd and even tile-row counts, one and
+    # several pair rows, two buckets in one launch
+    shapes = [(300, 700), (700, 300), (640, 960), (1024, 3072), (2048, 1024), (256, 256)]
+    ts = workloads.gen_tensors(workloads.Workload("symstore", shapes, 0.02, 23))
+    nsg.ns_set_gemm_cluster(cl)
+    try:
+        nsg.ns_set_symmetric_store(1)
+        a = run_ns(nsg, shapes, ts)
+        nsg.ns_set_symmetric_store(0)
+        b = run_ns(nsg, shapes, ts)
+    finally:
+        nsg.ns_set_symmetric_store(0)
+        nsg.ns_set_gemm_cluster(0)
+    for s_, x, y in zip(shapes, a, b):
+        assert torch.equal(x, y), (cl, s_)
+    for s_, t, y in zip(shapes[:3], ts, b):
+        assert rel_err(y, oracle_ns(t)) <= BF16_TOL, (cl, s_)
+
+
 @pytest.mark.parametrize("cl", [3])
 def test_cluster_and_single_cta_agree(cl):
     shapes = [(1024, 3072), (2048, 1024)]
