@@ -356,7 +356,7 @@ int ns_set_small_path(int enable);
 
 /* Tuning: how the bf16 path stores the symmetric matrices A = X X^T and
  * B = b A + c A^2 (SYRK: only the tiles that touch the upper triangle are
- * computed; Megatron-Core API page, the symmetric-Gram item of the issue).
+ * computed; [ISS], SYRK symmetric kernels).
  * Both tilings compute exactly the upper 256 x 256 pair blocks of each
  * m_pad x m_pad result, in full. mode = 0 (the default): only those blocks
  * are stored, and the products that read A or B (A*A, B*X) load the K-blocks
