@@ -560,8 +560,7 @@ def run_ours(args):
             # the pipeline overlaps the phases; only whole steps are timed
             ev[k][0].record(stream)
             step()
-            for j in (1, 2, 3):
-                ev[k][j].record(stream)
+            ev[k][1].record(stream)
             continue
         ev[k][0].record(stream)
         nsg.ns_pack_to_home(plan, rank_in, home_in, stream=stream)
@@ -581,8 +580,8 @@ def run_ours(args):
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
     pack_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
-    ns_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    unpack_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    ns_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev) if pipe is None else None
+    unpack_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev) if pipe is None else None
     n_mats = len(ns_shapes)
     value = job_value(n_mats, world, ms_step)
 

@@ -165,6 +165,15 @@ int ns_pipeline_run(ns_pipeline_t* pl, const void* const* rank_in, void* const* 
   // buffer, so the prologue reads the rank buffers and the pack to home_in is
   // skipped
   const bool fused_pack = p.layout == NS_LAYOUT_ROW_SHARD && p.shard_dim == 0;
+  if (pl->W == 1 && fused_pack && !pl->wave[0].buckets.empty() && gemm_buckets(pl->wave[0]) == 0) {
+    // every bucket runs as one CTA per matrix reading and writing the rank
+    // buffers: the whole call is one launch, issued on the caller's stream
+    // (nothing to overlap, so no fork onto the pipeline's streams and no join)
+    const Plan& wp = pl->wave[0];
+    std::vector<const void*> ins(wp.part.size(), nullptr);
+    std::vector<void*> outs(wp.part.size(), nullptr);
+    return small_bf16(wp, ins.data(), outs.data(), status, st, rank_in, rank_out);
+  }
   if (cudaEventRecord(ev[0], st) != cudaSuccess || cudaStreamWaitEvent(pd.mem, ev[0], 0) != cudaSuccess ||
       cudaStreamWaitEvent(pd.gemm, ev[0], 0) != cudaSuccess || cudaStreamWaitEvent(pd.out, ev[0], 0) != cudaSuccess)
     return NS_ERR_CUDA;

@@ -9,7 +9,8 @@ against the float64 oracle, and against the GEMM path it replaces.
 * the GEMM path (ns_set_small_path(False)) on the same inputs agrees;
 * a plan mixing small and GEMM buckets in one call;
 * the wave pipeline with small tensors read from and written to the rank
-  buffers equals the serial calls bit for bit.
+  buffers equals the serial calls bit for bit; with only small tensors it is
+  one launch on the caller's stream.
 """
 
 import numpy as np
@@ -121,3 +122,46 @@ def test_pipeline_with_small_tensors_in_rank_buffers(n_waves):
     for i in range(4, len(shapes)):
         y = torch.cat([ro2[r][offs[i]:offs[i + 1]] for r in range(S)]).reshape(ts[i].shape)
         assert rel_err(y, oracle_ns(ts[i])) <= BF16_TOL, shapes[i]
+
+
+def test_pipeline_all_small_one_launch_on_caller_stream():
+    # every bucket small: the pipeline call is the single small-kernel launch,
+    # ordered on the stream it is given (here a side stream), and equals the
+    # serial pack -> NS -> unpack bit for bit
+    w = workloads.small_16x128x256()
+    w.shapes = w.shapes + [(256, 64), (64, 512), (8, 8, 8), (128, 128)]
+    S, shapes = w.S, w.shapes
+    dev = torch.device("cuda:0")
+    ts = workloads.gen_tensors(w)
+    plan = nsg.ns_plan_create(shapes, S=S, shard_dim=0)
+    homes = plan.homes()
+    ho, hs, _ = plan.home_layout()
+    rank_in = [torch.cat([t.reshape(S, -1)[r] for t in ts]).to(dev) for r in range(S)]
+    hi1 = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    ho1 = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    ro1 = [torch.zeros_like(x) for x in rank_in]
+    ws = torch.empty(max(1, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+    nsg.ns_pack_to_home(plan, rank_in, hi1)
+    nsg.ns_orthogonalize_batched(plan, [hi1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))],
+                                 [ho1[homes[i]].data_ptr() + 2 * ho[i] for i in range(len(shapes))], ws)
+    nsg.ns_unpack_from_home(plan, ho1, ro1)
+    torch.cuda.synchronize()
+    pipe = nsg.ns_pipeline_create(plan, 2)
+    assert pipe.n_waves == 1
+    pws = torch.empty(max(1, pipe.workspace_bytes), dtype=torch.uint8, device=dev)
+    hi2 = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    ho2 = [torch.zeros(max(1, n), dtype=torch.bfloat16, device=dev) for n in hs]
+    ro2 = [torch.zeros_like(x) for x in rank_in]
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    nsg.ns_profile_read(reset=True)
+    with torch.cuda.stream(side):
+        nsg.ns_pipeline_run(pipe, rank_in, hi2, ho2, ro2, pws, stream=side)
+    side.synchronize()
+    launches, _ = nsg.ns_profile_read(reset=True)
+    assert nsg.ns_check_status(plan) == nsg.NS_OK
+    assert launches["small"] == 1 and sum(launches.values()) == 1, launches
+    for a in hi2 + ho2:
+        assert not a.any()
+    for a, b in zip(ro1, ro2):
+        assert torch.equal(a, b)
