@@ -15,6 +15,11 @@
 // from the transposed block, and the MMA takes that operand transposed. Both
 // CTAs' A rows lie in pair row q and their B rows in pair row tn, so the
 // choice is the same in both halves of every MMA.
+// In a diagonal pair tile of A*A (tn == q) each CTA's B rows are its own A
+// rows, in the same layout: only A is loaded and the MMA reads B from the A
+// stage. (The Gram's diagonal tiles could do the same, but the Gram does not
+// wait for its operands, and reading both from one stage made its MMAs a
+// little slower.)
 //
 // Synchronisation (all waits bounded):
 //   full[s]   leader only; count 1 (the leader's arrive.expect_tx of both
@@ -164,10 +169,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       // K-blocks left of the operand rows' diagonal pair block come transposed
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
+      const bool diag = PHASE == PH_A2B && tn == tm / 2;  // B rows == A rows
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
         const uint32_t full_l = map_to_rank(&full[stage], 0);
-        if (leader) mbar_arrive_expect_tx(&full[stage], PAIR_STAGE_BYTES);
+        if (leader) mbar_arrive_expect_tx(&full[stage], diag ? 2 * A_BYTES : PAIR_STAGE_BYTES);
         uint8_t* a_dst = sA + stage * A_BYTES;
         if (kb < kb_ta) {
 #pragma unroll
@@ -178,7 +184,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
         }
         uint8_t* b_dst = sB + stage * B_BYTES;
         const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
-        if (PHASE == PH_BX || kb < kb_tb) {
+        if (diag) {
+          // the A stage holds this CTA's B rows already
+        } else if (PHASE == PH_BX || kb < kb_tb) {
 #pragma unroll
           for (int j = 0; j < BN / 128; ++j)
             tma_load_3d_pair(b_dst + j * (64 * 128), &p.tmb[b], full_l, n0 + j * 64, kb * BK, mat);
@@ -211,11 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       const uint32_t d_tmem = tmem_base + acc * BN;
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
+      const bool diag = PHASE == PH_A2B && tn == tm / 2;
       for (int kb = 0; kb < kb_n; ++kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+        const uint32_t b_addr = diag ? a_addr : smem_u32(sB + stage * B_BYTES);
         const bool a_mn = kb < kb_ta;
         const bool b_mn = PHASE == PH_BX || kb < kb_tb;
         const uint32_t idesc = idesc_make(1u, 2 * BM, BN, a_mn, b_mn);

@@ -94,11 +94,6 @@ __global__ void __launch_bounds__(256) ns_scale_kernel(const __grid_constant__ P
   if (threadIdx.x == 0) *d.scale = static_cast<float>(1.0 / (sqrt(red[0]) + static_cast<double>(p.eps)));
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 __device__ __forceinline__ float sq8(const uint4& q) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   float acc = 0.0f;
