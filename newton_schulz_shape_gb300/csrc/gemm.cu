@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -158,34 +159,51 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       // K-blocks left of the operand rows' diagonal pair block come transposed
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
-      for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
-        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-        uint8_t* a_dst = sA + stage * A_BYTES;
-        uint8_t* b_dst = sB + stage * B_BYTES;
-        if (kb < kb_ta) {
+      // K-blocks [kb0, kb1) with one operand layout, fixed at compile time:
+      // layout choices made per K-block at run time slowed this single thread
+      // enough to leave the ring short of operands
+      auto load = [&](auto a_mn_c, auto b_mn_c, int kb0, int kb1) -> bool {
+        constexpr bool AMN = decltype(a_mn_c)::value, BMN = decltype(b_mn_c)::value;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) return false;
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          uint8_t* a_dst = sA + stage * A_BYTES;
+          uint8_t* b_dst = sB + stage * B_BYTES;
+          if (AMN) {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j)
-            tma_load_3d(a_dst + j * (64 * 128), &p.tmt[b], &full[stage], tm * BM + j * 64, kb * BK, mat);
-        } else {
-          tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
-        }
-        if (PHASE != PH_BX && kb >= kb_tb) {
-          // K-major rows: X (Gram), or A through the A operand's map (A*A)
-          const CUtensorMap* mb = PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b];
-          tma_load_3d(b_dst, mb, &full[stage], kb * BK, tn * BN, mat);
-          tma_load_3d(b_dst + 128 * 128, mb, &full[stage], kb * BK, tn * BN + 128, mat);
-        } else {
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_3d(a_dst + j * (64 * 128), &p.tmt[b], &full[stage], tm * BM + j * 64, kb * BK, mat);
+          } else {
+            tma_load_3d(a_dst, &p.tma[b], &full[stage], kb * BK, tm * BM, mat);
+          }
+          if (!BMN) {
+            // K-major rows: X (Gram), or A through the A operand's map (A*A)
+            const CUtensorMap* mb = PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b];
+            tma_load_3d(b_dst, mb, &full[stage], kb * BK, tn * BN, mat);
+            tma_load_3d(b_dst + 128 * 128, mb, &full[stage], kb * BK, tn * BN + 128, mat);
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(b_dst + j * (64 * 128), &p.tmb[b], &full[stage], tn * BN + j * 64, kb * BK, mat);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+        return true;
+      };
+      using T_ = std::true_type;
+      using F_ = std::false_type;
+      bool ok;
+      if (PHASE == PH_BX)
+        ok = load(T_{}, T_{}, 0, kb_ta) && load(F_{}, T_{}, kb_ta, kb_n);
+      else if (PHASE == PH_GRAM)
+        ok = load(F_{}, F_{}, 0, kb_n);
+      else
+        ok = load(T_{}, T_{}, 0, kb_ta) && load(F_{}, T_{}, kb_ta, kb_tb) && load(F_{}, F_{}, kb_tb, kb_n);
+      if (!ok) goto producer_done;
     }
   producer_done:
     if (*abort_flag) {
@@ -206,28 +224,42 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm_kernel(const __grid_consta
       const uint32_t d_tmem = tmem_base + acc * BN;
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
-      for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
-        tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
-        const bool a_mn = kb < kb_ta;
-        const bool b_mn = PHASE == PH_BX || kb < kb_tb;
-        const uint32_t idesc = idesc_make(1u, BM, BN, a_mn, b_mn);
+      // K-blocks [kb0, kb1) with one operand layout, fixed at compile time
+      auto run = [&](auto a_mn_c, auto b_mn_c, int kb0, int kb1) -> bool {
+        constexpr bool AMN = decltype(a_mn_c)::value, BMN = decltype(b_mn_c)::value;
+        constexpr uint32_t IDESC = idesc_make(1u, BM, BN, AMN, BMN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) return false;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / UK; ++k) {
-          const uint64_t ad = a_mn ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
-                                   : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
-          const uint64_t bd = b_mn ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
-                                   : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
-          mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = AMN ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
+                                    : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+            const uint64_t bd = BMN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
+            mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        mma_commit(&empty[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+        return true;
+      };
+      using T_ = std::true_type;
+      using F_ = std::false_type;
+      // at most three runs: both operands transposed, then A as rows, then both as rows
+      bool ok;
+      if (PHASE == PH_BX)
+        ok = run(T_{}, T_{}, 0, kb_ta) && run(F_{}, T_{}, kb_ta, kb_n);
+      else if (PHASE == PH_GRAM)
+        ok = run(F_{}, F_{}, 0, kb_n);
+      else
+        ok = run(T_{}, T_{}, 0, kb_ta) && run(F_{}, T_{}, kb_ta, kb_tb) && run(F_{}, F_{}, kb_tb, kb_n);
+      if (!ok) goto mma_done;
       mma_commit(&tfull[acc]);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;

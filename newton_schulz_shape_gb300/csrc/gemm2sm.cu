@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -170,36 +171,57 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
       const bool diag = PHASE == PH_A2B && tn == tm / 2;  // B rows == A rows
-      for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) goto producer_done;
-        const uint32_t full_l = map_to_rank(&full[stage], 0);
-        if (leader) mbar_arrive_expect_tx(&full[stage], diag ? 2 * A_BYTES : PAIR_STAGE_BYTES);
-        uint8_t* a_dst = sA + stage * A_BYTES;
-        if (kb < kb_ta) {
+      // K-blocks [kb0, kb1) with one operand layout (and, for DG, no B load),
+      // fixed at compile time: layout choices made per K-block at run time
+      // slowed this single thread enough to leave the ring short of operands
+      auto load = [&](auto a_mn_c, auto b_mn_c, auto dg_c, int kb0, int kb1) -> bool {
+        constexpr bool AMN = decltype(a_mn_c)::value, BMN = decltype(b_mn_c)::value, DG = decltype(dg_c)::value;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, lim)) return false;
+          const uint32_t full_l = map_to_rank(&full[stage], 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], DG ? 2 * A_BYTES : PAIR_STAGE_BYTES);
+          uint8_t* a_dst = sA + stage * A_BYTES;
+          if (AMN) {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j)
-            tma_load_3d_pair(a_dst + j * (64 * 128), &p.tmt[b], full_l, tm * BM + j * 64, kb * BK, mat);
-        } else {
-          tma_load_3d_pair(a_dst, &p.tma[b], full_l, kb * BK, tm * BM, mat);
-        }
-        uint8_t* b_dst = sB + stage * B_BYTES;
-        const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
-        if (diag) {
-          // the A stage holds this CTA's B rows already
-        } else if (PHASE == PH_BX || kb < kb_tb) {
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_3d_pair(a_dst + j * (64 * 128), &p.tmt[b], full_l, tm * BM + j * 64, kb * BK, mat);
+          } else {
+            tma_load_3d_pair(a_dst, &p.tma[b], full_l, kb * BK, tm * BM, mat);
+          }
+          // DG: the A stage holds this CTA's B rows already
+          if (!DG) {
+            uint8_t* b_dst = sB + stage * B_BYTES;
+            const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
+            if (BMN) {
 #pragma unroll
-          for (int j = 0; j < BN / 128; ++j)
-            tma_load_3d_pair(b_dst + j * (64 * 128), &p.tmb[b], full_l, n0 + j * 64, kb * BK, mat);
-        } else {
-          // K-major rows: X (Gram), or A through the A operand's map (A*A)
-          tma_load_3d_pair(b_dst, PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b], full_l, kb * BK, n0, mat);
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_3d_pair(b_dst + j * (64 * 128), &p.tmb[b], full_l, n0 + j * 64, kb * BK, mat);
+            } else {
+              // K-major rows: X (Gram), or A through the A operand's map (A*A)
+              tma_load_3d_pair(b_dst, PHASE == PH_GRAM ? &p.tmb[b] : &p.tma[b], full_l, kb * BK, n0, mat);
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+        return true;
+      };
+      using T_ = std::true_type;
+      using F_ = std::false_type;
+      bool ok;
+      if (PHASE == PH_BX)
+        ok = load(T_{}, T_{}, F_{}, 0, kb_ta) && load(F_{}, T_{}, F_{}, kb_ta, kb_n);
+      else if (PHASE == PH_GRAM)
+        ok = load(F_{}, F_{}, F_{}, 0, kb_n);
+      else if (diag)  // kb_ta == kb_tb here
+        ok = load(T_{}, T_{}, T_{}, 0, kb_ta) && load(F_{}, F_{}, T_{}, kb_ta, kb_n);
+      else
+        ok = load(T_{}, T_{}, F_{}, 0, kb_ta) && load(F_{}, T_{}, F_{}, kb_ta, kb_tb) &&
+             load(F_{}, F_{}, F_{}, kb_tb, kb_n);
+      if (!ok) goto producer_done;
     }
   producer_done:
     if (*abort_flag && leader) {
@@ -220,28 +242,46 @@ __global__ void __launch_bounds__(THREADS, 1) ns_gemm2sm_kernel(const __grid_con
       const int kb_ta = A_TRI && !p.mirror ? (tm / 2) * (2 * BM / BK) : 0;
       const int kb_tb = B_TRI && !p.mirror ? tn * (BN / BK) : 0;
       const bool diag = PHASE == PH_A2B && tn == tm / 2;
-      for (int kb = 0; kb < kb_n; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) goto mma_done;
-        tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-        const uint32_t b_addr = diag ? a_addr : smem_u32(sB + stage * B_BYTES);
-        const bool a_mn = kb < kb_ta;
-        const bool b_mn = PHASE == PH_BX || kb < kb_tb;
-        const uint32_t idesc = idesc_make(1u, 2 * BM, BN, a_mn, b_mn);
+      // K-blocks [kb0, kb1) with one operand layout, fixed at compile time so
+      // that the issuing thread spends no instructions choosing descriptors
+      auto run = [&](auto a_mn_c, auto b_mn_c, auto dg_c, int kb0, int kb1) -> bool {
+        constexpr bool AMN = decltype(a_mn_c)::value, BMN = decltype(b_mn_c)::value, DG = decltype(dg_c)::value;
+        constexpr uint32_t IDESC = idesc_make(1u, 2 * BM, BN, AMN, BMN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, lim)) return false;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = DG ? a_addr : smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / UK; ++k) {
-          const uint64_t ad = a_mn ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
-                                   : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
-          const uint64_t bd = b_mn ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
-                                   : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
-          mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = AMN ? sdesc_sw128(a_addr + k * (UK * 128), 64 * 128, 1024)
+                                    : sdesc_sw128(a_addr + k * (UK * 2), 16, 1024);
+            const uint64_t bd = BMN ? sdesc_sw128(b_addr + k * (UK * 128), 64 * 128, 1024)
+                                    : sdesc_sw128(b_addr + k * (UK * 2), 16, 1024);
+            mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair_mc(&empty[stage], 3);  // both CTAs' copies of the stage are free
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        mma_commit_pair_mc(&empty[stage], 3);  // both CTAs' copies of the stage are free
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+        return true;
+      };
+      using T_ = std::true_type;
+      using F_ = std::false_type;
+      // at most three runs: both operands transposed, then A as rows, then both as rows
+      bool ok;
+      if (PHASE == PH_BX)
+        ok = run(T_{}, T_{}, F_{}, 0, kb_ta) && run(F_{}, T_{}, F_{}, kb_ta, kb_n);
+      else if (PHASE == PH_GRAM)
+        ok = run(F_{}, F_{}, F_{}, 0, kb_n);
+      else if (diag)  // kb_ta == kb_tb here
+        ok = run(T_{}, T_{}, T_{}, 0, kb_ta) && run(F_{}, F_{}, T_{}, kb_ta, kb_n);
+      else
+        ok = run(T_{}, T_{}, F_{}, 0, kb_ta) && run(F_{}, T_{}, F_{}, kb_ta, kb_tb) &&
+             run(F_{}, F_{}, F_{}, kb_tb, kb_n);
+      if (!ok) goto mma_done;
       mma_commit_pair_mc(&tfull[acc], 3);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
