@@ -9,6 +9,11 @@
 // and B·X read their symmetric operands K-block by K-block: left of the
 // operand rows' diagonal pair block from the transposed, stored block
 // (MN-major loads, transposed MMA operand), elsewhere as rows (K-major).
+// The TMA producer and the MMA issuer therefore walk a tile's K-blocks in at
+// most three runs (both operands transposed, A as rows, both as rows), each
+// with its layout fixed at compile time: both are single threads that the
+// tensor pipe waits on, and choosing the layout per K-block at run time slowed
+// them measurably.
 //
 // One persistent kernel per phase, one CTA per SM, a 128 x 256 output tile per
 // work item, tiles of every shape bucket of the launch in one static schedule,
