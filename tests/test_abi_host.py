@@ -36,7 +36,8 @@ def test_header_constants_match_the_binding():
     # every enumerator of the header has the same value in the binding
     import re
     from newton_schulz_shape_gb300 import _lib
-    hdr = open(os.path.join(os.path.dirname(GOLD), "..", "include", "nsgb300.h")).read()
+    with open(os.path.join(os.path.dirname(GOLD), "..", "include", "nsgb300.h")) as f:
+        hdr = f.read()
     consts = dict((k, int(v)) for k, v in re.findall(r"\b(NS_[A-Z0-9_]+)\s*=\s*(-?\d+)", hdr))
     assert len(consts) >= 17
     for k, v in consts.items():

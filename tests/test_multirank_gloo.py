@@ -112,5 +112,6 @@ def test_two_rank_plan_agreement_exchange_and_timing(tmp_path):
     msgs = []
     for r in range(WORLD):
         if os.path.exists(err + f".{r}"):
-            msgs.append(open(err + f".{r}").read())
+            with open(err + f".{r}") as f:
+                msgs.append(f.read())
     assert all(p.exitcode == 0 for p in procs), "\n".join(msgs)
