@@ -257,7 +257,9 @@ int ns_unpack_from_home(ns_plan_t* plan, const void* const* home_bufs, int S, in
  * rank buffer, the prologue reads the rank buffers directly and the last B*X
  * launch of each wave writes the results straight into rank_out, so home_in
  * and home_out are left untouched (a wave whose last launch cannot address
- * all its matrices still stages its results in home_out). workspace
+ * all its matrices still stages its results in home_out). When every bucket
+ * of such a plan runs as one CTA per matrix, the whole call is that one
+ * launch, issued on `stream` itself. workspace
  * holds two wave workspaces (ns_pipeline_info), 256-byte aligned. The call
  * is ordered after prior work on `stream`, and later work on `stream` waits
  * for all of it. The first run on a device creates the pipeline's streams
