@@ -172,7 +172,7 @@ def gemm_kernel_for(kind: str, cluster_mode: int, shapes=()):
     if kind == "small":
         return "ns_small_kernel", "small.cu"
     even = all(((view_mn(s)[0] + 127) // 128) % 2 == 0 for s in shapes if not is_small(s))
-    mode = cluster_mode if cluster_mode else (3 if kind == "gram" or even else 1)
+    mode = cluster_mode if cluster_mode else (3 if kind in ("gram", "a2b") or even else 1)
     if mode == 3:
         return f"ns_gemm2sm_kernel<{kind}>", "gemm2sm.cu"
     return f"ns_gemm_kernel<{kind}>", "gemm.cu"

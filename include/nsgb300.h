@@ -338,8 +338,8 @@ int ns_test_set_route_home(ns_plan_t* plan, int tensor, int home);
 /* Tuning: how the bf16 GEMM phases use the tensor cores. cl = 1: one CTA per
  * 128 x 256 tile (tcgen05 cta_group::1); cl = 3: clusters of two CTAs running
  * the 2-SM MMA (cta_group::2) on 256 x 256 tiles, each SM holding half of
- * each operand; cl = 0 (default) picks 3 for the Gram phase, and 3 for A*A
- * and B*X when every bucket has an even number of 128-row tile rows (else 1):
+ * each operand; cl = 0 (default) picks 3 for the Gram and A*A phases, and 3
+ * for B*X when every bucket has an even number of 128-row tile rows (else 1):
  * the fastest measured per phase. The paired mode applies to launches whose
  * buckets all have at least two 128-row tile rows; others use 1. Any other
  * value is NS_ERR_ARG. Process-wide; all modes give bitwise-identical

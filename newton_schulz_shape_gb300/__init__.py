@@ -259,7 +259,7 @@ def ns_profile_read(reset: bool = False):
 
 
 def ns_set_gemm_cluster(cl: int) -> None:
-    """GEMM tiling: 0 automatic (2-SM MMA for the Gram, and for A*A and B*X when
+    """GEMM tiling: 0 automatic (2-SM MMA for the Gram and A*A, and for B*X when
     every bucket has an even number of 128-row tile rows), 1 single CTA,
     3 2-SM MMA."""
     check(lib.ns_set_gemm_cluster(cl), "ns_set_gemm_cluster")

@@ -43,11 +43,11 @@ int pick_cl(const Plan& p, size_t b0, size_t b1, int phase) {
   }
   if (const int f = gemm_cluster_override()) return f;
   // Measured (interleaved runs on one plan): the 2-SM MMA is faster for the
-  // Gram (K = n) everywhere, and for A*A and B*X when every bucket has an even
+  // Gram (K = n) and A*A everywhere, and for B*X when every bucket has an even
   // number of tile rows (GPT-style and Llama-shaped: 16 and 32 rows); with an
   // odd count the spare half of the last pair makes the 1-SM kernel faster
-  // for those two (MoE 1408-row experts: 11 rows).
-  if (phase != nsk::PH_GRAM)
+  // for B*X (MoE 1408-row experts: 11 rows).
+  if (phase == nsk::PH_BX)
     for (size_t bi = b0; bi < b1; ++bi)
       if ((p.buckets[bi].m_pad / nsk::GEMM_BM) % 2) return 1;
   return 3;

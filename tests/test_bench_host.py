@@ -32,17 +32,20 @@ def test_executed_flops_even_tile_rows():
 
 
 def test_executed_flops_odd_tile_rows():
-    # m = 1408: 11 tile rows (odd) -> Gram on 6 pairs with a spare half:
-    # 6 + 5 + ... + 1 = 21 pair tiles = 42 CTA tiles of 128 x 256;
-    # A*A on single CTAs: rows r take 6 - floor(r / 2) tiles -> 41 tiles;
+    # m = 1408: 11 tile rows (odd) -> Gram and A*A on 6 pairs with a spare
+    # half: 6 + 5 + ... + 1 = 21 pair tiles = 42 CTA tiles of 128 x 256;
     # B*X on single CTAs: 11 x 8 tiles, exactly m x n
     m, n = 1408, 2048
     ex = bench.executed_flops_by_kind([(m, n)], 1)
     assert ex["gram"] == 2 * 128 * 256 * n * 42
-    assert ex["a2b"] == 2 * 128 * 256 * m * 41
+    assert ex["a2b"] == 2 * 128 * 256 * m * 42
     assert ex["bx"] == 2 * m * m * n
     assert bench.gemm_kernel_for("gram", 0, [(m, n)])[0] == "ns_gemm2sm_kernel<gram>"
+    assert bench.gemm_kernel_for("a2b", 0, [(m, n)])[0] == "ns_gemm2sm_kernel<a2b>"
     assert bench.gemm_kernel_for("bx", 0, [(m, n)])[0] == "ns_gemm_kernel<bx>"
+    # forced single CTAs: A*A rows r take 6 - floor(r / 2) tiles -> 41 tiles
+    ex1 = bench.executed_flops_by_kind([(m, n)], 1, 1)
+    assert ex1["a2b"] == 2 * 128 * 256 * m * 41
     assert bench.gemm_kernel_for("a2b", 0, [(2048, 8192)])[0] == "ns_gemm2sm_kernel<a2b>"
 
 
