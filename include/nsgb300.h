@@ -43,7 +43,7 @@ enum {
   NS_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed               */
   NS_ERR_TIMEOUT = -6,       /* a kernel's bounded wait ran out (device status)  */
   NS_ERR_DEVICE_CHECK = -7,  /* a kernel refused an out-of-range index           */
-  NS_ERR_UNSUPPORTED = -8,   /* mode or device not supported by this build      */
+  NS_ERR_UNSUPPORTED = -8,   /* mode or device not supported by this library    */
   NS_ERR_WORKSPACE = -9      /* workspace missing, too small or misaligned       */
 };
 

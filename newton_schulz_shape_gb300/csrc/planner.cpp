@@ -700,7 +700,7 @@ const char* ns_status_string(int status) {
     case NS_ERR_CUDA: return "CUDA error";
     case NS_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
     case NS_ERR_DEVICE_CHECK: return "a kernel refused an out-of-range index";
-    case NS_ERR_UNSUPPORTED: return "not supported by this build or device";
+    case NS_ERR_UNSUPPORTED: return "not supported by this library or device";
     case NS_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     default: return "unknown status";
   }

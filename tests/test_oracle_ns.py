@@ -179,7 +179,7 @@ def test_useful_flops():
     assert ons.useful_flops((256, 128), 5) == 104857600
 
 
-# --- the per-matrix error measure every parity verdict goes through --------
+# --- the per-matrix error measure every parity check goes through ----------
 # Hand-worked values of ||y - y_ref||_F / ||y_ref||_F (and ||y||_F when
 # y_ref = 0). Each case is chosen so that a plausible slip gives a different
 # number: the squared ratio, the wrong denominator (||y|| instead of
